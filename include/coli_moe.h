@@ -1,0 +1,216 @@
+/*
+ * coli_moe — forward pass of one sparse Mixture-of-Experts layer on one GB300
+ * (sm_103a), behind a plain C ABI.
+ *
+ * The layer (the "four atomic operations" of the Colibri overview page,
+ * trdm.cn/news/527833, section 2.1):
+ *   1. router:   l = x·W_r^T (+ b), p = softmax(l) over the E experts
+ *                (gating formula softmax(x·w_gate + b_gate), wzjinhao.cn
+ *                "Colibri 是什么", section 3.2);
+ *   2. top-k:    the k largest logits (ties: lower expert index first),
+ *                gates renormalised over the k chosen: g_j = p_j / sum p;
+ *   3. dispatch: assignments grouped by expert id with a stable counting
+ *                sort (discosf.com "Colibri 不是一只蜂鸟", section 4.2);
+ *   4. experts:  per non-empty expert a SwiGLU FFN,
+ *                y = (silu(x·Wg^T) * (x·Wu^T))·Wd^T, no biases (w1 = gate,
+ *                w3 = up, w2 = down: overview page section 3.1); experts
+ *                without tokens are never read (wzjinhao.cn section 2.3);
+ *   5. combine:  y[t] = sum_j g[t][j] * y_perm[row(t, j)], back in token
+ *                order (mhpn.cn "Colibri 一个被低估的…", section 2.3).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless the name says host. `stream` is a
+ *     cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Every matrix is row-major. Weights use the nn.Linear "[out][in]"
+ *     layout, reduction index contiguous: W_r [E][d], W_gate/W_up [E][f][d],
+ *     W_down [E][d][f]. int4 (COLI_I4G128): signed two's-complement nibbles,
+ *     the low nibble holding the even reduction index, [..][cols/2] bytes,
+ *     with one bf16 scale per 128 consecutive reduction indices of a row,
+ *     [..][cols/128]; w = q * s (group-wise int4: wth2jhl.online Colibri deep
+ *     dive, section 7.3).
+ *   - Return value: COLI_OK (0) or a negative coli_status, errno style
+ *     (mhpn.cn page, section 3.3). A message goes to the caller's `err`
+ *     buffer where the call has one (truncated to err_len, NUL-terminated)
+ *     and always to the calling thread's coli_last_error().
+ *   - Arguments are validated before anything is launched. Problems found
+ *     on the device (an expert id out of range, a bounded wait that ran out)
+ *     never trap: the kernel skips the access, latches the first error code
+ *     in a per-device status word and returns; coli_device_status() reports
+ *     it.
+ *   - Launches are asynchronous on `stream`; buffers must stay alive until
+ *     the stream work completes. No entry point but create, destroy, the
+ *     host-buffer forward and the status query synchronises.
+ */
+#ifndef COLI_MOE_H
+#define COLI_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  COLI_OK = 0,
+  COLI_EINVAL = -1,       /* bad argument (null pointer, size, dtype, alignment) */
+  COLI_ENOMEM = -2,       /* device allocation failed (create only) */
+  COLI_ECUDA = -3,        /* a CUDA runtime/driver call failed */
+  COLI_EUNSUPPORTED = -4, /* valid but not implemented combination */
+  COLI_EDEVICE = -5,      /* a kernel found bad data (e.g. expert id >= E) */
+  COLI_ETIMEOUT = -6      /* a bounded device-side wait ran out */
+} coli_status;
+
+typedef enum { COLI_F32 = 0, COLI_BF16 = 1, COLI_I4G128 = 2 } coli_dtype;
+
+/* Expert-FFN path. AUTO picks DECODE when the mean number of rows per expert
+ * (T*k/E) is at most 64, else PREFILL. DECODE streams each active expert's
+ * weights once (tensor-core MMA fed straight from HBM); PREFILL is the
+ * TMA + tcgen05/TMEM grouped GEMM. Both give the same routing and the same
+ * outputs within rounding. F32 layers always use the CUDA-core path; int4
+ * experts always use DECODE. */
+typedef enum { COLI_PATH_AUTO = 0, COLI_PATH_DECODE = 1, COLI_PATH_PREFILL = 2 } coli_path;
+
+typedef struct {
+  int32_t d_model;         /* d: multiple of 64 (int4: of 128) */
+  int32_t d_ff;            /* f: multiple of 64 (int4: of 128) */
+  int32_t n_experts;       /* E: 1..256 */
+  int32_t top_k;           /* k: 1..min(E, 8) */
+  int32_t max_tokens;      /* largest T any forward will see (workspace size) */
+  int32_t act_dtype;       /* coli_dtype of x, y and W_r: F32 or BF16 */
+  int32_t weight_dtype;    /* F32 (with F32 activations), BF16 or I4G128 (with BF16) */
+  int32_t has_router_bias; /* 0 or 1 */
+  int32_t path;            /* coli_path */
+} coli_moe_config;
+
+typedef struct {
+  const void* w_router;  /* [E][d] act dtype */
+  const float* b_router; /* [E] f32, or NULL when has_router_bias == 0 */
+  const void* w_gate;    /* [E][f][d]   (int4: [E][f][d/2] bytes) */
+  const void* w_up;      /* [E][f][d]   (int4: [E][f][d/2] bytes) */
+  const void* w_down;    /* [E][d][f]   (int4: [E][d][f/2] bytes) */
+  const void* s_gate;    /* int4 only: bf16 [E][f][d/128], else NULL */
+  const void* s_up;      /* int4 only: bf16 [E][f][d/128], else NULL */
+  const void* s_down;    /* int4 only: bf16 [E][d][f/128], else NULL */
+} coli_moe_weights;
+
+typedef struct coli_moe coli_moe;
+
+/* ---- library ---------------------------------------------------------- */
+const char* coli_version(void);
+const char* coli_status_string(int status);
+/* Message of the last failing call made by this thread ("" if none). */
+const char* coli_last_error(void);
+/* First device-side error latched since the last query on the current
+ * device (COLI_OK if none); synchronises `stream`, then clears the word. */
+int coli_device_status(void* stream, char* err, size_t err_len);
+
+/* ---- layer handle (lifecycle after wzjinhao.cn section 4.3: load, run,
+ * free the run state before the model) ----------------------------------- */
+
+/* Copies and repacks the weights into a handle-owned layout (gate/up rows
+ * interleaved in blocks of 64; int4 nibbles reordered for in-register
+ * dequantisation) and allocates every workspace buffer a forward of up to
+ * max_tokens tokens needs (the memory budget is fixed at load time:
+ * wzjinhao.cn section 2.3). Synchronises `stream` before returning, so the
+ * caller may free its weight buffers afterwards. On failure *out is NULL and
+ * nothing is leaked. */
+int coli_moe_create(const coli_moe_config* cfg, const coli_moe_weights* weights, void* stream,
+                    coli_moe** out, char* err, size_t err_len);
+
+/* y[T][d] = layer(x[T][d]) in the act dtype, 0 <= T <= max_tokens. x and y
+ * must be 16-byte aligned and must not overlap. Allocates nothing and never
+ * synchronises the host (zero allocation inside inference: mhpn.cn section
+ * 3.2). Calls on one handle must not overlap in time. */
+int coli_moe_forward(coli_moe* h, const void* x, int32_t T, void* y, void* stream, char* err,
+                     size_t err_len);
+
+/* Same layer with HOST buffers x_host[T][d] and y_host[T][d] (act dtype):
+ * copies x in, runs the forward, copies y out and synchronises `stream`
+ * before returning. Pinned host memory gives the fastest copies. */
+int coli_moe_forward_host(coli_moe* h, const void* x_host, int32_t T, void* y_host, void* stream,
+                          char* err, size_t err_len);
+
+/* Synchronises `stream` and reports the first device-side error latched
+ * since the last query (COLI_EDEVICE / COLI_ETIMEOUT) or COLI_OK. */
+int coli_moe_device_status(coli_moe* h, void* stream, char* err, size_t err_len);
+
+/* Device pointers to the last forward's intermediates (valid until the next
+ * forward on this handle): topk_idx [T][k] i32, topk_w [T][k] f32, gap [T]
+ * f32 (l_(k) - l_(k+1), +inf when k == E), counts [E], offsets [E+1],
+ * row_token [T*k], assign_row [T*k] (all i32). Any output may be NULL. */
+int coli_moe_debug_buffers(const coli_moe* h, const int32_t** topk_idx, const float** topk_w,
+                           const float** gap, const int32_t** counts, const int32_t** offsets,
+                           const int32_t** row_token, const int32_t** assign_row);
+
+/* Path (coli_path, never AUTO) a forward of T tokens takes on this handle. */
+int coli_moe_path_for(const coli_moe* h, int32_t T);
+
+/* Per-stage timing with CUDA events recorded on the forward's stream.
+ * Stages: 0 router, 1 dispatch, 2 expert gate/up, 3 expert down, 4 combine.
+ * coli_moe_stage_times synchronises on the last recorded event, adds the
+ * elapsed milliseconds of every timed forward since the last call into
+ * ms[0..n), the number of timed forwards into *n_forwards and the number of
+ * kernel launches into *n_launches, then resets the sums. */
+int coli_moe_set_timing(coli_moe* h, int enable);
+int coli_moe_stage_times(coli_moe* h, float* ms, int n, int32_t* n_forwards, int64_t* n_launches);
+
+/* Frees the handle; all stream work on it must have finished. NULL is a no-op. */
+void coli_moe_destroy(coli_moe* h);
+
+/* ---- exposed stages ----------------------------------------------------- */
+
+/* Router + softmax + top-k + renormalisation (overview page sections 2.1 and
+ * 3.2; gating formula wzjinhao.cn section 3.2; the router emits only k ids
+ * and k scores per token: discosf.com section 2.1).
+ * x [T][d], w_router [E][d] (act dtype), b_router [E] f32 or NULL ->
+ * topk_idx [T][k] i32 (descending logit, lower index first on ties),
+ * topk_w [T][k] f32 (renormalised gates), gap [T] f32 or NULL.
+ * Logits are fp32 dot products (+ bias in fp32). Needs
+ * coli_route_scratch_bytes(T, E) bytes of device scratch (0 when E <= 32;
+ * scratch may then be NULL). */
+size_t coli_route_scratch_bytes(int32_t T, int32_t E);
+int coli_route_topk(const void* x, const void* w_router, const float* b_router, int32_t T,
+                    int32_t d, int32_t E, int32_t k, int32_t act, int32_t* topk_idx,
+                    float* topk_w, float* gap, void* scratch, size_t scratch_bytes,
+                    void* stream);
+
+/* Dispatch (discosf.com section 4.2 counting sort; overview section 3.3
+ * token-to-expert map and expert offsets): counts [E], offsets [E+1]
+ * (exclusive prefix), row_token [T*k], assign_row [T*k] and the gathered
+ * rows x_perm [T*k][d] = x[row_token[r]]. Rows of one expert keep token
+ * order, so the result is unique and bit-exact. Ids outside [0, E) are
+ * skipped and latch COLI_EDEVICE. Needs coli_permute_scratch_bytes(T, k, E)
+ * bytes of device scratch (256-byte aligned). */
+size_t coli_permute_scratch_bytes(int32_t T, int32_t k, int32_t E);
+int coli_permute(const int32_t* topk_idx, const void* x, int32_t T, int32_t d, int32_t E,
+                 int32_t k, int32_t act, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                 int32_t* assign_row, void* x_perm, void* scratch, size_t scratch_bytes,
+                 void* stream);
+
+/* Expert FFN on grouped rows with the handle's weights (overview section 3.3
+ * per-expert GEMM; only experts with rows are touched). x_perm [n_rows][d]
+ * (act dtype), offsets [E+1] as produced by coli_permute (n_rows ==
+ * offsets[E] <= max_tokens * k) -> y_perm [n_rows][d] f32. Uses the
+ * handle's workspace: do not overlap with a forward on the same handle. */
+int coli_expert_ffn(const coli_moe* h, const void* x_perm, const int32_t* offsets,
+                    int32_t n_rows, float* y_perm, void* stream);
+
+/* Combine (overview section 2.1 weighted merge; mhpn.cn section 2.3 copy back
+ * in token order): y[t] = sum_{j ascending} topk_w[t][j] *
+ * y_perm[assign_row[t*k+j]], summed in fp32, written in `out` dtype
+ * (bf16 by round-to-nearest-even). */
+int coli_combine(const float* y_perm, const int32_t* assign_row, const float* topk_w,
+                 int32_t T, int32_t k, int32_t d, int32_t out, void* y, void* stream);
+
+/* ---- fault-handling self-test ------------------------------------------ */
+/* Launches one block that waits on a shared-memory barrier nothing will ever
+ * complete, giving up after spin_limit polls: it latches COLI_ETIMEOUT and
+ * returns, leaving the context usable. Tests the bounded-wait machinery. */
+int coli_selftest_bounded_wait(int32_t spin_limit, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* COLI_MOE_H */
