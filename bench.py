@@ -1,0 +1,382 @@
+"""Benchmark of one sparse MoE layer forward on GB300.
+
+Default workload: the Mixtral-8x7B-shaped layer at a decode batch (T=32,
+d=4096, E=8, k=2, d_ff=14336, bf16), whose expert FFN streams the 2.8 GB of
+activated expert weights once per forward. Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+    python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+A "step" is one whole forward (router, dispatch, expert FFN, combine) over the
+workload's T tokens with inputs resident in HBM. Multi-GPU runs are replicas
+(every rank holds the layer and processes its own T tokens; no collective on
+the data path), so scaling is weak and value = all ranks' tokens / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s on 1 GB300; achieved HBM GB/s or TC TFLOPS vs chip peak"
+STAGES = ["router", "dispatch", "expert_gateup", "expert_down", "combine"]
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--config", default="mixtral_decode")
+    p.add_argument("--impl", default="coli", choices=["coli", "reference"])
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="budget of the oracle CPU-baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_desc(s):
+    return (f"{s.name}: T={s.T}, d={s.d}, E={s.E}, k={s.k}, d_ff={s.f}, act={s.act}, "
+            f"experts={s.wdt}" + (", Zipf router bias" if s.bias == "zipf" else ""))
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def aggregate(local_tokens: int, local_seconds: float, world: int):
+    """(total tokens over ranks, max seconds over ranks); needs an initialised
+    process group when world > 1."""
+    if world == 1:
+        return local_tokens, local_seconds
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    n = torch.tensor([float(local_tokens)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return int(n.item()), float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def oracle_sample(s, layer, budget_s: float):
+    """Time the oracle (as it stands, one thread) on a bounded sample of this
+    workload's tokens; returns (tokens/s, tokens timed, seconds)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.moe_forward(layer, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f, tokens=[0])
+    one = max(time.perf_counter() - t0, 1e-6)
+    n = int(max(1, min(s.T, budget_s / one)))
+    tokens = np.arange(n, dtype=np.int32) % s.T
+    t0 = time.perf_counter()
+    oracle.moe_forward(layer, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f, tokens=tokens)
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from mixture_experts_gb300 import inputs
+    s = inputs.CONFIGS[args.config]
+    layer = inputs.make_layer(s, seed=0)
+    per_step = []
+    budget = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    n_total, t_total = 0, 0.0
+    for i in range(args.warmup + args.steps):
+        tps, n, dt = oracle_sample(s, layer, budget)
+        if i >= args.warmup:
+            per_step.append(dt)
+            n_total += n
+            t_total += dt
+    value = n_total / t_total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t_total / max(1, len(per_step)), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
+        "config": {"workload": workload_desc(s)},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n_total // max(1, args.steps)} of the {s.T} tokens per "
+                                   f"step, whole layer per token, single thread"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="coli_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, smax, pw = [], [], []
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                pw.append(float(r[3]))
+            except ValueError:
+                pass
+            for i, n in enumerate(names):
+                if r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------- traffic record
+def traffic_record(config: str, kernel_file: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    summary, if the kernel source is unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh).get(config)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "mixture_experts_gb300", "csrc", kernel_file)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec["bytes_per_launch"] if rec.get("source_sha") == sha else None
+
+
+# ---------------------------------------------------------------- GPU leg
+def run_coli(args):
+    import numpy as np
+    import torch
+    import mixture_experts_gb300 as moe
+    from mixture_experts_gb300 import inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    moe.build()
+    s = inputs.CONFIGS[args.config]
+    host = inputs.make_layer(s, seed=0)
+    if rank > 0:  # replicas: same weights, this rank's own tokens
+        host["x"] = inputs.random_rows(s.T, s.d, s.act_code, seed=1000 + rank)
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in host.items()}
+    layer = moe.MoELayer(s.d, s.f, s.E, s.k, s.T, s.act_code, s.w_code, dev)
+    x = dev["x"]
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    path = {moe.PATH_DECODE: "decode", moe.PATH_PREFILL: "prefill"}[layer.path_for(s.T)]
+
+    weight_bytes = sum(v.numel() * v.element_size() for k, v in host.items()
+                       if k.startswith(("w_gate", "w_up", "w_down", "s_")) and v is not None)
+    flush = weight_bytes < 2 * L2_BYTES
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if flush else None
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        layer(x, y)
+    barrier()
+
+    # ---- timed region: K forwards with stage timing on the launching stream
+    moe.coli_moe_set_timing(layer.h, True)
+    moe.coli_moe_stage_times(layer.h)  # reset sums
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    if flush:
+        per = []
+        for _ in range(args.steps):
+            scrub.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            layer(x, y)
+            b.record(stream)
+            b.synchronize()
+            per.append(a.elapsed_time(b))
+        elapsed_ms = sum(per)
+    else:
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            layer(x, y)
+        b.record(stream)
+        barrier()
+        elapsed_ms = a.elapsed_time(b)
+    barrier()
+    clk = clocks.stop()
+    stage_ms, n_fwd, n_launch = moe.coli_moe_stage_times(layer.h)
+    moe.coli_moe_set_timing(layer.h, False)
+    tokens, seconds = aggregate(s.T * args.steps, elapsed_ms / 1e3, world)
+    value = tokens / seconds
+
+    # ---- dominant kernel roofline
+    pk, pk_src = peaks()
+    dbg = layer.debug(s.T)
+    counts = dbg["counts"].cpu().numpy()
+    active = int((counts > 0).sum())
+    n_rows = int(counts.sum())
+    avg = [m / max(1, n_fwd) for m in stage_ms]
+    gu_ms = avg[2]
+    if path == "decode":
+        if s.wdt == "i4g128":
+            per_expert = 2 * s.f * s.d // 2 + 2 * s.f * (s.d // 128) * 2
+        else:
+            per_expert = 2 * s.f * s.d * (4 if s.wdt == "f32" else 2)
+        alg = per_expert * active
+        achieved = alg / (gu_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"],
+                "traffic": traffic_record(args.config, "k_ffn_dec.cu"),
+                "kernel": "k_dec_gateup (expert gate/up projection + SwiGLU)",
+                "algorithmic_bytes_per_launch": alg,
+                "unit_work": f"{per_expert} B of gate/up weights per activated expert x "
+                             f"{active} activated experts",
+                "peak_source": f"{pk_src} hbm_gbs"}
+    else:
+        flops = 2.0 * n_rows * s.d * 2 * s.f
+        achieved = flops / (gu_ms / 1e3) / 1e12
+        peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic_record(args.config, "k_ffn_tc.cu"),
+                "kernel": "k_tc_gemm (gate/up grouped GEMM + SwiGLU)",
+                "algorithmic_flops_per_launch": flops,
+                "peak_source": f"{pk_src} bf16_tflops_sustained"}
+    ffn_ms = avg[2] + avg[3]
+    if path == "decode":
+        if s.wdt == "i4g128":
+            all_bytes = active * (3 * s.f * s.d // 2 + 3 * s.f * (s.d // 128) * 2)
+        else:
+            all_bytes = active * 3 * s.f * s.d * 2
+        roof["expert_ffn_total"] = {"achieved_gbs": all_bytes / (ffn_ms / 1e3) / 1e9,
+                                    "frac": all_bytes / (ffn_ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+
+    # ---- end to end through the public API with host buffers
+    xh = host["x"].pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    for _ in range(3):
+        layer.forward_host(xh, yh)
+    e2e_steps = max(10, min(args.steps, 500))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        layer.forward_host(xh, yh)
+    e2e_s = time.perf_counter() - t0
+    e_tokens, e_seconds = aggregate(s.T * e2e_steps, e2e_s, world)
+    io_bytes = s.T * s.d * (4 if s.act == "f32" else 2)
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            tps, n, dt = oracle_sample(s, host, args.cpu_seconds)
+            cpu = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                   "sample": f"{n} of the {s.T} tokens of one step, whole layer per token "
+                             f"({dt:.1f} s, one thread)"}
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if s.act == "bf16" else "f32",
+            "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
+            "config": {"workload": workload_desc(s), "path": path,
+                       "parallelism": f"replicas x{world}",
+                       "l2": ("L2 flushed between steps" if flush else
+                              f"inputs larger than L2: {weight_bytes / 1e9:.2f} GB of expert "
+                              f"weights streamed per step"),
+                       "active_experts": active},
+            "roofline": roof,
+            "stage_ms": dict(zip(STAGES, [round(m, 5) for m in avg])),
+            "cpu_baseline": cpu,
+            "e2e": {"value": e_tokens / e_seconds, "unit": "tokens/s",
+                    "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes},
+            "gpu_launches": int(n_launch * args.steps / max(1, n_fwd)),
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    layer.close()
+    return line
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_coli(args)
+
+
+if __name__ == "__main__":
+    main()

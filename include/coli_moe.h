@@ -143,6 +143,13 @@ int coli_moe_debug_buffers(const coli_moe* h, const int32_t** topk_idx, const fl
                            const float** gap, const int32_t** counts, const int32_t** offsets,
                            const int32_t** row_token, const int32_t** assign_row);
 
+/* Copies the last forward's intermediates (as listed above; T is that
+ * forward's token count) into caller-owned device buffers, asynchronously on
+ * `stream`. Any destination may be NULL. */
+int coli_moe_copy_debug(const coli_moe* h, int32_t T, int32_t* topk_idx, float* topk_w,
+                        float* gap, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                        int32_t* assign_row, void* stream);
+
 /* Path (coli_path, never AUTO) a forward of T tokens takes on this handle. */
 int coli_moe_path_for(const coli_moe* h, int32_t T);
 
@@ -167,9 +174,9 @@ void coli_moe_destroy(coli_moe* h);
  * topk_idx [T][k] i32 (descending logit, lower index first on ties),
  * topk_w [T][k] f32 (renormalised gates), gap [T] f32 or NULL.
  * Logits are fp32 dot products (+ bias in fp32). Needs
- * coli_route_scratch_bytes(T, E) bytes of device scratch (0 when E <= 32;
+ * coli_route_scratch_bytes(T, d, E) bytes of device scratch (0 when E <= 32;
  * scratch may then be NULL). */
-size_t coli_route_scratch_bytes(int32_t T, int32_t E);
+size_t coli_route_scratch_bytes(int32_t T, int32_t d, int32_t E);
 int coli_route_topk(const void* x, const void* w_router, const float* b_router, int32_t T,
                     int32_t d, int32_t E, int32_t k, int32_t act, int32_t* topk_idx,
                     float* topk_w, float* gap, void* scratch, size_t scratch_bytes,

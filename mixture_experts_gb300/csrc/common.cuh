@@ -1,0 +1,122 @@
+// Device helpers shared by the coli_moe kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define COLI_DEV __device__ __forceinline__
+
+namespace coli {
+
+// Status codes latched on the device (same values as coli_status).
+constexpr int kErrDevice = -5;
+constexpr int kErrTimeout = -6;
+
+// Every bounded wait gives up after this long (a healthy wait takes µs).
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+// First error wins; later errors leave the word untouched.
+COLI_DEV void latch_error(int* status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+COLI_DEV uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- bf16 <-> f32 --------------------------------------------------------
+COLI_DEV float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+COLI_DEV float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+template <typename T>
+COLI_DEV float to_f32(T v);
+template <>
+COLI_DEV float to_f32<float>(float v) { return v; }
+template <>
+COLI_DEV float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// Two floats -> packed bf16x2 (low half = a), round to nearest even.
+COLI_DEV uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// ---- global loads ----------------------------------------------------------
+// Streamed once (expert weights): bypass L1, 256-byte L2 fetch granule.
+COLI_DEV uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+// Re-read by neighbouring warps (activations): keep in L1.
+COLI_DEV uint4 ldg_keep(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// ---- warp-level tensor-core MMA (m16n8k16, bf16 in, fp32 accumulate) --------
+COLI_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                             uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---- shared memory / mbarrier ---------------------------------------------
+COLI_DEV uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+COLI_DEV void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+COLI_DEV void mbar_arrive(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
+COLI_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+          bar),
+      "r"(bytes)
+      : "memory");
+}
+
+COLI_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete; false once
+// timeout_ns has passed (the caller latches kErrTimeout and unwinds).
+COLI_DEV bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns = kWaitTimeoutNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+COLI_DEV uint32_t lane_id() { return threadIdx.x & 31u; }
+
+}  // namespace coli

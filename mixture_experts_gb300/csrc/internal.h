@@ -1,0 +1,84 @@
+// Host-side launchers shared between the translation units of libcoli_moe.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace coli {
+
+enum { DT_F32 = 0, DT_BF16 = 1, DT_I4G128 = 2 };
+
+// Per-device status word (first device-side error wins).
+int* device_status_ptr();  // nullptr if the symbol address cannot be taken
+
+// ---- router (A1) ------------------------------------------------------------
+size_t route_scratch_bytes(int T, int d, int E);
+cudaError_t launch_route(const void* x, const void* w_r, const float* b_r, int T, int d, int E,
+                         int k, int act, int32_t* topk_idx, float* topk_w, float* gap,
+                         void* scratch, cudaStream_t st, int* n_launches);
+
+// ---- dispatch (A2) ------------------------------------------------------------
+size_t permute_scratch_bytes(int T, int k, int E);
+cudaError_t launch_permute(const int32_t* topk_idx, const void* x, int T, int d, int E, int k,
+                           int act, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                           int32_t* assign_row, void* x_perm, void* scratch, cudaStream_t st,
+                           int* status, int* n_launches);
+
+// ---- expert FFN (A3) ----------------------------------------------------------
+// Weights in the handle's layout: gate/up rows interleaved in blocks of 64
+// ([E][2f][d]: rows 128b..128b+63 are gate features 64b.., the next 64 the
+// matching up features); down [E][d][f]. int4: bytes with each 32-bit word
+// holding the 8 reduction indices 8w..8w+7 as nibbles (even indices in the
+// low half-word, odd in the high), scales bf16 [rows][cols/128].
+struct FfnWeights {
+  int wdt;
+  const void* w_gu;
+  const __nv_bfloat16* s_gu;
+  const void* w_dn;
+  const __nv_bfloat16* s_dn;
+};
+
+// Tensor-core decode path: streams the weights of every non-empty expert once.
+// steps = reduction steps of one down row (f/32 bf16, f/128 int4)
+int dec_down_splits(int n_rows, int E, int d, int steps, int n_warps);
+cudaError_t launch_dec_gateup(const FfnWeights& w, const __nv_bfloat16* x_perm,
+                              const int32_t* offsets, int E, int d, int f, __nv_bfloat16* H,
+                              int grid, cudaStream_t st);
+cudaError_t launch_dec_down(const FfnWeights& w, const __nv_bfloat16* H, const int32_t* offsets,
+                            int E, int d, int f, int splits, float* y_part, size_t part_stride,
+                            int grid, cudaStream_t st);
+int dec_blocks_per_sm();
+
+// fp32 CUDA-core path (f32 activations and weights).
+cudaError_t launch_f32_ffn(const float* w_gu, const float* w_dn, const float* x_perm,
+                           const int32_t* offsets, int n_rows, int E, int d, int f, float* H,
+                           float* y_perm, cudaStream_t st, int* n_launches);
+
+// Prefill path: TMA + tcgen05/TMEM grouped GEMM (bf16 weights).
+struct TcPlan;  // defined in k_ffn_tc.cu
+bool tc_supported(int d, int f);
+cudaError_t tc_plan_create(TcPlan** plan, const void* w_gu, const void* w_dn, int E, int d, int f,
+                           int max_rows);
+void tc_plan_destroy(TcPlan* plan);
+// H[rows][f] = silu(x_perm Wg^T) * (x_perm Wu^T) per expert group (bf16).
+cudaError_t launch_tc_gateup(TcPlan* plan, const void* x_perm, const int32_t* offsets, void* H,
+                             int n_rows, cudaStream_t st, int* status);
+// y_perm[rows][d] = H Wd^T per expert group (f32).
+cudaError_t launch_tc_down(TcPlan* plan, const void* H, const int32_t* offsets, float* y_perm,
+                           int n_rows, cudaStream_t st, int* status);
+
+// ---- combine (A4) and helpers ----------------------------------------------------
+cudaError_t launch_combine(const float* y_part, int splits, size_t part_stride,
+                           const int32_t* assign_row, const float* topk_w, int T, int k, int d,
+                           int out_dt, void* y, cudaStream_t st);
+cudaError_t launch_reduce_splits(const float* y_part, int splits, size_t part_stride,
+                                 int n_rows, int d, float* y_perm, cudaStream_t st);
+cudaError_t launch_repack(const void* src_gate, const void* src_up, const void* src_down,
+                          const void* sg, const void* su, const void* sd, int wdt, int E, int d,
+                          int f, void* dst_gu, void* dst_sgu, void* dst_dn, void* dst_sdn,
+                          cudaStream_t st);
+cudaError_t launch_selftest_wait(int spin_limit, int* status, cudaStream_t st);
+
+}  // namespace coli

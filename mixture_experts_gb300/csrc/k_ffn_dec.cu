@@ -1,0 +1,408 @@
+// A3, decode path: per-expert SwiGLU FFN for groups of a few rows.
+//
+// With a handful of tokens per expert the FFN is bound by streaming each
+// active expert's weights once (the "sparse GEMM" of the overview page,
+// trdm.cn section 3.3, measured there as a fraction of memory bandwidth;
+// batch-union — each expert read once however many tokens chose it — from
+// the wth2jhl.online deep dive, section 4.3). Experts with no rows are never
+// read (wzjinhao.cn section 2.3).
+//
+// Design (swap-AB): the weight rows are the M side of a warp-level
+// m16n8k16 bf16 tensor-core MMA and the (<= 32) token rows of the expert are
+// the N side, so every weight byte is loaded exactly once, straight from HBM
+// into registers with 16-byte streaming loads, and used as the A fragment
+// without passing through shared memory. The reduction index is permuted
+// consistently on both operands (a dot product does not depend on the order
+// of its terms): in every 32-wide step, lane q = lane % 4 owns the 8
+// contiguous indices 8q..8q+7 of its two rows, which feed the k-slots
+// {2q, 2q+1, 2q+8, 2q+9} of two MMAs; the token fragment is loaded with the
+// same 16-byte pattern from the activations.
+//
+// int4 experts: a step is one 128-wide scale group and lane q owns indices
+// 32q..32q+31 (16 bytes). The weights were reordered at create so each 32-bit
+// word holds 8 consecutive indices with even ones in the low half-word; one
+// LOP3 per pair turns two nibbles into bf16 (136 + q), an HSUB2 removes the
+// 136, and the group's partial sums are scaled by the row's bf16 scale in
+// fp32: sum_g s_g * sum_{i in g} q_i x_i, i.e. exactly w = q * s.
+//
+// Gate and up tiles of the same 16 features are processed by one warp so
+// silu(gate) * up is applied in registers (h is rounded to bf16 for the down
+// projection). The down projection splits its reduction into `splits`
+// slices when there are too few (expert, 32-row) items to fill the GPU; the
+// slices are summed in fixed order later (no float atomics).
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace coli {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarpsPerBlock = kThreads / 32;
+template <bool INT4>
+constexpr int kMaxRowsPerPass = INT4 ? 16 : 32;  // token rows per weight pass
+
+COLI_DEV uint4 zero4() { return make_uint4(0u, 0u, 0u, 0u); }
+
+// Two nibbles (bits 0-3 and 16-19 of w >> 4j) -> bf16x2 integers q.
+COLI_DEV uint32_t nib_pair(uint32_t w, int j) {
+  uint32_t v = w >> (4 * j);
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(v), "r"(0x000F000Fu), "r"(0x43084308u));
+  // (v & 0x000F000F) ^ 0x43084308  ->  bf16 (136 + q) in each half
+  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&r);
+  const __nv_bfloat162 off = __floats2bfloat162_rn(136.f, 136.f);
+  x = __hsub2(x, off);
+  return *reinterpret_cast<uint32_t*>(&x);
+}
+
+COLI_DEV uint4 dequant_word(uint32_t w) {
+  return make_uint4(nib_pair(w, 0), nib_pair(w, 1), nib_pair(w, 2), nib_pair(w, 3));
+}
+
+COLI_DEV uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// acc[m][n] += A(tile m) x B(n) over one 8-index chunk held as bf16 uint4s:
+// ar/ar8 rows r and r+8 of tile m, b the token fragment.
+template <int NT>
+COLI_DEV void mma_chunk(float (&acc)[2][NT][4], const uint4 (&ar)[2], const uint4 (&ar8)[2],
+                        const uint4 (&b)[NT]) {
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      mma_bf16_16816(acc[m][n], ar[m].x, ar8[m].x, ar[m].y, ar8[m].y, b[n].x, b[n].y);
+      mma_bf16_16816(acc[m][n], ar[m].z, ar8[m].z, ar[m].w, ar8[m].w, b[n].z, b[n].w);
+    }
+}
+
+// One warp: two 16-row weight tiles x NT 8-token tiles over steps [s0, s1).
+// wrow[m][h]: byte pointer to row (r + 8h) of tile m, already offset by this
+// lane's 16-byte column; a step advances 64 bytes. xrow[n]: byte pointer to
+// this lane's token row of tile n (offset by the lane's column), nullptr for
+// padding rows. srow[m][h]: int4 scales of the same rows (one per step).
+template <bool INT4, int NT>
+COLI_DEV void mainloop(const uint8_t* const (&wrow)[2][2], const __nv_bfloat16* const (&srow)[2][2],
+                       const uint8_t* const (&xrow)[NT], int s0, int s1,
+                       float (&acc)[2][NT][4]) {
+  if constexpr (!INT4) {
+    // loads in flight per lane: U * (4 + NT) x 16 bytes
+    constexpr int U = NT == 1 ? 4 : (NT == 2 ? 2 : 1);
+    int s = s0;
+    for (; s + U <= s1; s += U) {
+      uint4 a[U][2][2], b[U][NT];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) a[u][m][h] = ldg_stream(wrow[m][h] + (s + u) * 64);
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+          b[u][n] = xrow[n] ? ldg_keep(xrow[n] + (s + u) * 64) : zero4();
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint4 ar[2] = {a[u][0][0], a[u][1][0]};
+        const uint4 ar8[2] = {a[u][0][1], a[u][1][1]};
+        mma_chunk<NT>(acc, ar, ar8, b[u]);
+      }
+    }
+    for (; s < s1; ++s) {
+      uint4 ar[2], ar8[2], b[NT];
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        ar[m] = ldg_stream(wrow[m][0] + s * 64);
+        ar8[m] = ldg_stream(wrow[m][1] + s * 64);
+      }
+#pragma unroll
+      for (int n = 0; n < NT; ++n) b[n] = xrow[n] ? ldg_keep(xrow[n] + s * 64) : zero4();
+      mma_chunk<NT>(acc, ar, ar8, b);
+    }
+  } else {
+    // a step = one 128-index group; the lane's x fragment is 64 bytes
+    // (32 consecutive indices) at byte offset 256*s + 64*q.
+    constexpr int U = NT == 1 ? 2 : 1;
+    for (int s = s0; s < s1; s += U) {
+      uint4 a[U][2][2];
+      float sc[U][2][2];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int ss = s + u < s1 ? s + u : s;  // clamp; duplicate work is discarded
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            a[u][m][h] = ldg_stream(wrow[m][h] + ss * 64);
+            sc[u][m][h] = __bfloat162float(srow[m][h][ss]);
+          }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (s + u >= s1) break;
+        float g[2][NT][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) g[m][n][c] = 0.f;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 bv[NT];
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+            bv[n] = xrow[n] ? ldg_keep(xrow[n] + (s + u) * 256 + v * 16) : zero4();
+          const uint4 ar[2] = {dequant_word(word_of(a[u][0][0], v)),
+                               dequant_word(word_of(a[u][1][0], v))};
+          const uint4 ar8[2] = {dequant_word(word_of(a[u][0][1], v)),
+                                dequant_word(word_of(a[u][1][1], v))};
+          mma_chunk<NT>(g, ar, ar8, bv);
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            acc[m][n][0] = fmaf(sc[u][m][0], g[m][n][0], acc[m][n][0]);
+            acc[m][n][1] = fmaf(sc[u][m][0], g[m][n][1], acc[m][n][1]);
+            acc[m][n][2] = fmaf(sc[u][m][1], g[m][n][2], acc[m][n][2]);
+            acc[m][n][3] = fmaf(sc[u][m][1], g[m][n][3], acc[m][n][3]);
+          }
+      }
+    }
+  }
+}
+
+struct DecArgs {
+  const uint8_t* w;              // gate/up or down weights (bytes)
+  const __nv_bfloat16* s;        // int4 scales or nullptr
+  const __nv_bfloat16* x;        // activations [rows][K] (x_perm or H)
+  const int32_t* offsets;        // [E+1]
+  int E, K;                      // experts, reduction length
+  int rows_per_expert;           // weight rows per expert (2f or d)
+  int f;                         // features (gate/up)
+  int d;                         // outputs (down)
+  int splits;                    // reduction slices (down)
+  __nv_bfloat16* H;              // gate/up output [rows][f]
+  float* y_part;                 // down output [splits][rows][d]
+  size_t part_stride;            // elements between slices
+};
+
+// Byte offset of the lane's 16-byte column within a row at step 0.
+template <bool INT4>
+COLI_DEV size_t row_bytes(int K) {
+  return INT4 ? static_cast<size_t>(K) / 2 : static_cast<size_t>(K) * 2;
+}
+
+template <bool INT4, int NT>
+COLI_DEV void gateup_chunk(const DecArgs& A, int e, int n0, int row0, int nrows) {
+  const int lane = threadIdx.x & 31, r = lane >> 2, q = lane & 3;
+  const size_t rb = row_bytes<INT4>(A.K);
+  const int gs = A.K / 128;
+  // interleaved rows: gate feature n -> 128*(n/64) + n%64, up -> +64
+  const size_t gbase = static_cast<size_t>(e) * A.rows_per_expert + 128 * (n0 / 64) + (n0 % 64);
+  const uint8_t* wrow[2][2];
+  const __nv_bfloat16* srow[2][2];
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const size_t row = gbase + 64 * m + r + 8 * h;
+      wrow[m][h] = A.w + row * rb + q * 16;
+      srow[m][h] = INT4 ? A.s + row * gs : nullptr;
+    }
+  const uint8_t* xrow[NT];
+  const int xlane = INT4 ? q * 64 : q * 16;
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    const int j = 8 * n + r;
+    xrow[n] = j < nrows ? reinterpret_cast<const uint8_t*>(A.x + static_cast<size_t>(row0 + j) * A.K) + xlane
+                        : nullptr;
+  }
+  float acc[2][NT][4];
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[m][n][c] = 0.f;
+  const int steps = INT4 ? A.K / 128 : A.K / 32;
+  mainloop<INT4, NT>(wrow, srow, xrow, 0, steps, acc);
+  // acc[0] = gate, acc[1] = up: rows (features) r, r+8; columns (tokens) 2q, 2q+1
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = 8 * n + 2 * q + (c & 1);
+      if (j >= nrows) continue;
+      const int feat = n0 + r + ((c & 2) ? 8 : 0);
+      const float a = acc[0][n][c], u = acc[1][n][c];
+      const float hval = a / (1.f + expf(-a)) * u;
+      A.H[static_cast<size_t>(row0 + j) * A.f + feat] = __float2bfloat16_rn(hval);
+    }
+}
+
+template <bool INT4, int NT>
+COLI_DEV void down_chunk(const DecArgs& A, int e, int o0, int split, int row0, int nrows) {
+  const int lane = threadIdx.x & 31, r = lane >> 2, q = lane & 3;
+  const size_t rb = row_bytes<INT4>(A.K);
+  const int gs = A.K / 128;
+  const uint8_t* wrow[2][2];
+  const __nv_bfloat16* srow[2][2];
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const size_t row = static_cast<size_t>(e) * A.rows_per_expert + o0 + 16 * m + r + 8 * h;
+      wrow[m][h] = A.w + row * rb + q * 16;
+      srow[m][h] = INT4 ? A.s + row * gs : nullptr;
+    }
+  const uint8_t* xrow[NT];
+  const int xlane = INT4 ? q * 64 : q * 16;
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    const int j = 8 * n + r;
+    xrow[n] = j < nrows ? reinterpret_cast<const uint8_t*>(A.x + static_cast<size_t>(row0 + j) * A.K) + xlane
+                        : nullptr;
+  }
+  float acc[2][NT][4];
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[m][n][c] = 0.f;
+  const int steps = INT4 ? A.K / 128 : A.K / 32;
+  const int s0 = static_cast<int>(static_cast<long>(steps) * split / A.splits);
+  const int s1 = static_cast<int>(static_cast<long>(steps) * (split + 1) / A.splits);
+  mainloop<INT4, NT>(wrow, srow, xrow, s0, s1, acc);
+  float* out = A.y_part + static_cast<size_t>(split) * A.part_stride;
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int j = 8 * n + 2 * q + (c & 1);
+        if (j >= nrows) continue;
+        const int o = o0 + 16 * m + r + ((c & 2) ? 8 : 0);
+        out[static_cast<size_t>(row0 + j) * A.d + o] = acc[m][n][c];
+      }
+}
+
+// Persistent: warp w of the grid takes items w, w + W, w + 2W, ...; an item
+// is (expert, 16 features); consecutive items share the expert so the warps
+// of a block re-read the same activation rows from L1.
+template <bool INT4>
+__global__ void __launch_bounds__(kThreads, 2) k_dec_gateup(const DecArgs A) {
+  const int W = gridDim.x * kWarpsPerBlock;
+  const int per_e = A.f / 16;
+  const int items = A.E * per_e;
+  for (int it = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); it < items; it += W) {
+    const int e = it / per_e, n0 = (it % per_e) * 16;
+    const int r0 = A.offsets[e], r1 = A.offsets[e + 1];
+    for (int row0 = r0; row0 < r1; row0 += kMaxRowsPerPass<INT4>) {
+      const int nrows = min(kMaxRowsPerPass<INT4>, r1 - row0);
+      switch ((nrows + 7) / 8) {
+        case 1: gateup_chunk<INT4, 1>(A, e, n0, row0, nrows); break;
+        case 2: gateup_chunk<INT4, 2>(A, e, n0, row0, nrows); break;
+        case 3: if constexpr (!INT4) gateup_chunk<INT4, 3>(A, e, n0, row0, nrows); break;
+        default: if constexpr (!INT4) gateup_chunk<INT4, 4>(A, e, n0, row0, nrows); break;
+      }
+    }
+  }
+}
+
+// Item = (slice, expert, 32 outputs); the slice is outermost so neighbouring
+// warps read the same part of H.
+template <bool INT4>
+__global__ void __launch_bounds__(kThreads, 2) k_dec_down(const DecArgs A) {
+  const int W = gridDim.x * kWarpsPerBlock;
+  const int per_e = A.d / 32;
+  const int per_split = A.E * per_e;
+  const int items = per_split * A.splits;
+  for (int it = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); it < items; it += W) {
+    const int split = it / per_split, rem = it % per_split;
+    const int e = rem / per_e, o0 = (rem % per_e) * 32;
+    const int r0 = A.offsets[e], r1 = A.offsets[e + 1];
+    for (int row0 = r0; row0 < r1; row0 += kMaxRowsPerPass<INT4>) {
+      const int nrows = min(kMaxRowsPerPass<INT4>, r1 - row0);
+      switch ((nrows + 7) / 8) {
+        case 1: down_chunk<INT4, 1>(A, e, o0, split, row0, nrows); break;
+        case 2: down_chunk<INT4, 2>(A, e, o0, split, row0, nrows); break;
+        case 3: if constexpr (!INT4) down_chunk<INT4, 3>(A, e, o0, split, row0, nrows); break;
+        default: if constexpr (!INT4) down_chunk<INT4, 4>(A, e, o0, split, row0, nrows); break;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+int dec_blocks_per_sm() {
+  int a = 0, b = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_dec_gateup<false>, kThreads, 0) !=
+      cudaSuccess)
+    a = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_dec_gateup<true>, kThreads, 0) !=
+      cudaSuccess)
+    b = 1;
+  int c = a < b ? a : b;
+  return c < 1 ? 1 : c;
+}
+
+int dec_down_splits(int n_rows, int E, int d, int steps, int n_warps) {
+  const int active = n_rows < E ? n_rows : E;  // at most this many non-empty experts
+  if (active <= 0) return 1;
+  const long items = static_cast<long>(active) * (d / 32);
+  long s = (2L * n_warps + items - 1) / items;
+  if (s > 8) s = 8;
+  if (s > steps) s = steps;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
+cudaError_t launch_dec_gateup(const FfnWeights& w, const __nv_bfloat16* x_perm,
+                              const int32_t* offsets, int E, int d, int f, __nv_bfloat16* H,
+                              int grid, cudaStream_t st) {
+  DecArgs A{};
+  A.w = static_cast<const uint8_t*>(w.w_gu);
+  A.s = w.s_gu;
+  A.x = x_perm;
+  A.offsets = offsets;
+  A.E = E;
+  A.K = d;
+  A.rows_per_expert = 2 * f;
+  A.f = f;
+  A.d = d;
+  A.splits = 1;
+  A.H = H;
+  if (w.wdt == DT_I4G128) k_dec_gateup<true><<<grid, kThreads, 0, st>>>(A);
+  else k_dec_gateup<false><<<grid, kThreads, 0, st>>>(A);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dec_down(const FfnWeights& w, const __nv_bfloat16* H, const int32_t* offsets,
+                            int E, int d, int f, int splits, float* y_part, size_t part_stride,
+                            int grid, cudaStream_t st) {
+  DecArgs A{};
+  A.w = static_cast<const uint8_t*>(w.w_dn);
+  A.s = w.s_dn;
+  A.x = H;
+  A.offsets = offsets;
+  A.E = E;
+  A.K = f;
+  A.rows_per_expert = d;
+  A.f = f;
+  A.d = d;
+  A.splits = splits;
+  A.y_part = y_part;
+  A.part_stride = part_stride;
+  if (w.wdt == DT_I4G128) k_dec_down<true><<<grid, kThreads, 0, st>>>(A);
+  else k_dec_down<false><<<grid, kThreads, 0, st>>>(A);
+  return cudaGetLastError();
+}
+
+}  // namespace coli

@@ -1,0 +1,292 @@
+// A1: router linear + softmax + top-k + renormalised gates.
+//
+// Gating is softmax(x·W_r^T + b) over the E experts (wzjinhao.cn "Colibri
+// 是什么", section 3.2); the k largest are kept and their gates renormalised
+// (overview page trdm.cn, section 2.1 "Top-k Selection"); the router hands on
+// only k ids and k scores per token (discosf.com page, section 2.1).
+//
+// E <= 32: one fused kernel, one warp per token. Lanes split the reduction
+// index, every lane ends with all E logits in registers (xor-butterfly sums
+// are bitwise identical in every lane), and lane e ranks expert e against
+// the others: rank(e) = #{e' : l[e'] > l[e] or (l[e'] == l[e] and e' < e)}.
+// E > 32: logits are too many for one warp's registers and W_r too large to
+// re-read per token, so a tiled fp32 kernel first writes partial dot products
+// over token x expert x reduction-slice tiles (fixed slice order, no atomics),
+// then a warp-per-token kernel sums the slices, keeps E/32 logits per lane in
+// registers and takes k+1 rounds of warp arg-max (larger value, then lower
+// index) for the top-k and the k-th/(k+1)-th gap.
+//
+// Logits are fp32 dot products (bf16 inputs widened exactly) plus the bias in
+// fp32. Gates use expf with max-subtraction (same page, section 3.2).
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace coli {
+namespace {
+
+constexpr int kWarps = 8;
+
+COLI_DEV void load8(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+COLI_DEV void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x);
+  v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+  v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z);
+  v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+}
+
+COLI_DEV bool beats(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Value of the lane that holds `rank` (exactly one lane does).
+COLI_DEV float from_rank(int my_rank, float my_val, int rank) {
+  const unsigned m = __ballot_sync(0xffffffffu, my_rank == rank);
+  return __shfl_sync(0xffffffffu, my_val, __ffs(m) - 1);
+}
+
+template <typename TA, int EMAX>
+__global__ void __launch_bounds__(kWarps * 32)
+    k_route_fused(const TA* __restrict__ x, const TA* __restrict__ w, const float* __restrict__ b,
+                  int T, int d, int E, int k, int32_t* __restrict__ topk_idx,
+                  float* __restrict__ topk_w, float* __restrict__ gap) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float acc[EMAX];
+#pragma unroll
+  for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
+  const TA* xr = x + static_cast<size_t>(t) * d;
+  for (int i = lane * 8; i < d; i += 256) {
+    float xv[8];
+    load8(xr + i, xv);
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+      if (e < E) {
+        float wv[8];
+        load8(w + static_cast<size_t>(e) * d + i, wv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[e] = fmaf(xv[j], wv[j], acc[e]);
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < EMAX; ++e) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+    if (e < E && b != nullptr) acc[e] += b[e];
+  }
+  // lane e owns expert e
+  float le = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < EMAX; ++e)
+    if (e == lane) le = acc[e];
+  int rank = 0;
+#pragma unroll
+  for (int e = 0; e < EMAX; ++e)
+    if (e < E && beats(acc[e], e, le, lane)) ++rank;
+  const bool mine = lane < E;
+  if (!mine) rank = 1 << 20;
+  const float m = from_rank(rank, le, 0);
+  const bool sel = mine && rank < k;
+  const float ex = sel ? expf(le - m) : 0.f;
+  float den = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  if (sel) {
+    topk_idx[static_cast<size_t>(t) * k + rank] = lane;
+    topk_w[static_cast<size_t>(t) * k + rank] = ex / den;
+  }
+  if (gap != nullptr) {
+    float g = INFINITY;
+    if (k < E) g = from_rank(rank, le, k - 1) - from_rank(rank, le, k);
+    if (lane == 0) gap[t] = g;
+  }
+}
+
+// ---- E > 32 ---------------------------------------------------------------------
+constexpr int kTT = 16;   // tokens per tile
+constexpr int kTE = 64;   // experts per tile
+constexpr int kKS = 512;  // reduction slice per CTA
+constexpr int kKC = 32;   // reduction chunk staged in shared memory
+
+template <typename TA>
+__global__ void __launch_bounds__(128)
+    k_route_partial(const TA* __restrict__ x, const TA* __restrict__ w, int T, int d, int E,
+                    float* __restrict__ part) {
+  __shared__ float xs[kTT][kKC + 1];
+  __shared__ float ws[kTE][kKC + 1];
+  const int t0 = blockIdx.x * kTT, e0 = blockIdx.y * kTE, k0 = blockIdx.z * kKS;
+  const int k1 = min(d, k0 + kKS);
+  const int tid = threadIdx.x;
+  const int tp = tid >> 4;   // tokens 2tp, 2tp+1
+  const int eq = tid & 15;   // experts 4eq..4eq+3
+  float acc[2][4] = {};
+  for (int kk = k0; kk < k1; kk += kKC) {
+    for (int i = tid; i < kTT * kKC; i += 128) {
+      const int r = i / kKC, c = i % kKC, t = t0 + r;
+      xs[r][c] = (t < T) ? to_f32(x[static_cast<size_t>(t) * d + kk + c]) : 0.f;
+    }
+    for (int i = tid; i < kTE * kKC; i += 128) {
+      const int r = i / kKC, c = i % kKC, e = e0 + r;
+      ws[r][c] = (e < E) ? to_f32(w[static_cast<size_t>(e) * d + kk + c]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int c = 0; c < kKC; ++c) {
+      const float xa = xs[2 * tp][c], xb = xs[2 * tp + 1][c];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float wv = ws[4 * eq + j][c];
+        acc[0][j] = fmaf(xa, wv, acc[0][j]);
+        acc[1][j] = fmaf(xb, wv, acc[1][j]);
+      }
+    }
+    __syncthreads();
+  }
+  float* dst = part + static_cast<size_t>(blockIdx.z) * T * E;
+#pragma unroll
+  for (int a = 0; a < 2; ++a) {
+    const int t = t0 + 2 * tp + a;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + 4 * eq + j;
+      if (e < E) dst[static_cast<size_t>(t) * E + e] = acc[a][j];
+    }
+  }
+}
+
+template <int PER_LANE>
+__global__ void __launch_bounds__(kWarps * 32)
+    k_route_select(const float* __restrict__ part, int slices, const float* __restrict__ b,
+                   int T, int E, int k, int32_t* __restrict__ topk_idx,
+                   float* __restrict__ topk_w, float* __restrict__ gap) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float l[PER_LANE];
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) {
+    const int e = lane + 32 * i;
+    float v = -INFINITY;
+    if (e < E) {
+      v = 0.f;
+      for (int s = 0; s < slices; ++s) v += part[(static_cast<size_t>(s) * T + t) * E + e];
+      if (b != nullptr) v += b[e];
+    }
+    l[i] = v;
+  }
+  unsigned taken = 0;  // bit i: slot i of this lane already selected
+  float best0 = 0.f, prev = 0.f, den = 0.f;
+  float sel_val[8];
+  int sel_idx[8];
+  const int rounds = min(k + 1, E);
+  for (int r = 0; r < rounds; ++r) {
+    float bv = -INFINITY;
+    int bi = 1 << 30;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !(taken & (1u << i)) && beats(l[i], e, bv, bi)) {
+        bv = l[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (beats(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (r < k) {
+      sel_val[r] = bv;
+      sel_idx[r] = bi;
+    }
+    if (r == 0) best0 = bv;
+    if (r == k - 1) prev = bv;
+    if (r == k && gap != nullptr && lane == 0) gap[t] = prev - bv;
+  }
+  if (k == E && gap != nullptr && lane == 0) gap[t] = INFINITY;
+  // gates: exp(l_j - l_max) / sum_j' exp(l_j' - l_max), j ascending
+  for (int j = 0; j < k; ++j) den += expf(sel_val[j] - best0);
+  if (lane < k) {
+    float v = 0.f;
+    int id = 0;
+    for (int j = 0; j < k; ++j)
+      if (j == lane) {
+        v = sel_val[j];
+        id = sel_idx[j];
+      }
+    topk_idx[static_cast<size_t>(t) * k + lane] = id;
+    topk_w[static_cast<size_t>(t) * k + lane] = expf(v - best0) / den;
+  }
+}
+
+int slices_for(int d) { return (d + kKS - 1) / kKS; }
+
+}  // namespace
+
+size_t route_scratch_bytes(int T, int d, int E) {
+  if (E <= 32 || T <= 0) return 0;
+  const size_t n = static_cast<size_t>(slices_for(d)) * T * E * sizeof(float);
+  return (n + 255) & ~static_cast<size_t>(255);
+}
+
+cudaError_t launch_route(const void* x, const void* w_r, const float* b_r, int T, int d, int E,
+                         int k, int act, int32_t* topk_idx, float* topk_w, float* gap,
+                         void* scratch, cudaStream_t st, int* n_launches) {
+  if (T == 0) return cudaSuccess;
+  const dim3 block(kWarps * 32);
+  const dim3 grid((T + kWarps - 1) / kWarps);
+  if (E <= 32) {
+#define COLI_ROUTE_FUSED(TA, EM)                                                             \
+  k_route_fused<TA, EM><<<grid, block, 0, st>>>(static_cast<const TA*>(x),                 \
+                                               static_cast<const TA*>(w_r), b_r, T, d, E, k, \
+                                               topk_idx, topk_w, gap)
+    if (act == DT_F32) {
+      if (E <= 8) COLI_ROUTE_FUSED(float, 8);
+      else if (E <= 16) COLI_ROUTE_FUSED(float, 16);
+      else COLI_ROUTE_FUSED(float, 32);
+    } else {
+      if (E <= 8) COLI_ROUTE_FUSED(__nv_bfloat16, 8);
+      else if (E <= 16) COLI_ROUTE_FUSED(__nv_bfloat16, 16);
+      else COLI_ROUTE_FUSED(__nv_bfloat16, 32);
+    }
+#undef COLI_ROUTE_FUSED
+    if (n_launches) *n_launches += 1;
+    return cudaGetLastError();
+  }
+  float* part = static_cast<float*>(scratch);
+  const int S = slices_for(d);
+  const dim3 pgrid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE, S);
+  if (act == DT_F32)
+    k_route_partial<float><<<pgrid, 128, 0, st>>>(static_cast<const float*>(x),
+                                                   static_cast<const float*>(w_r), T, d, E, part);
+  else
+    k_route_partial<__nv_bfloat16><<<pgrid, 128, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_r), T, d, E,
+        part);
+  if (E <= 64)
+    k_route_select<2><<<grid, block, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap);
+  else if (E <= 128)
+    k_route_select<4><<<grid, block, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap);
+  else
+    k_route_select<8><<<grid, block, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap);
+  if (n_launches) *n_launches += 2;
+  return cudaGetLastError();
+}
+
+}  // namespace coli

@@ -1,0 +1,215 @@
+"""CUDA path vs the oracle, element by element, through the C ABI (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_gb300 as moe
+import oracle
+from mixture_experts_gb300 import inputs
+from parity import (TOL, check_dispatch, check_routing, cuda_layer, host_dict, make_handle,
+                    oracle_routing, rel_err, y_to_f64)
+
+pytestmark = pytest.mark.gpu
+
+S = inputs.MoEShape
+SMALL = {
+    "tiny_fp32": inputs.CONFIGS["tiny_fp32"],
+    "decode_bf16": S("decode_bf16", T=24, d=512, E=8, k=2, f=384),
+    "prefill_bf16": S("prefill_bf16", T=600, d=512, E=8, k=2, f=768),
+    "int4": S("int4", T=40, d=1024, E=16, k=4, f=256, wdt="i4g128"),
+    "int4_big_groups": S("int4_big_groups", T=70, d=256, E=2, k=1, f=256, wdt="i4g128"),
+    "skew_small": S("skew_small", T=2048, d=256, E=64, k=4, f=128, bias="zipf"),
+    "e256_sparse": S("e256_sparse", T=50, d=256, E=256, k=8, f=128),
+    "e1_k1": S("e1_k1", T=5, d=128, E=1, k=1, f=64),
+    "k_eq_e": S("k_eq_e", T=9, d=128, E=4, k=4, f=64),
+    "hot_expert": S("hot_expert", T=50, d=256, E=8, k=2, f=128, bias="hot0"),
+    "one_token": S("one_token", T=1, d=256, E=8, k=2, f=128),
+    "fp32_e64": S("fp32_e64", T=33, d=192, E=64, k=3, f=64, act="f32", wdt="f32"),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    moe.build()
+    assert torch.cuda.is_available()
+
+
+def run_layer(s, lay, path=moe.PATH_AUTO):
+    dev = cuda_layer(lay)
+    layer = make_handle(s, dev, path=path)
+    y = layer(dev["x"])
+    dbg = layer.debug(s.T)
+    torch.cuda.synchronize()
+    assert layer.status() == moe.COLI_OK
+    return layer, y, host_dict(dbg)
+
+
+def check_layer(s, lay, y, dbg, tokens=None):
+    idx, w, gap, inner = oracle_routing(s, lay)
+    near = check_routing(dbg["topk_idx"], dbg["topk_w"], idx, w, gap, inner)
+    check_dispatch(dbg, idx, near, s.E)
+    assert np.allclose(dbg["gap"][~near], gap[~near], rtol=0, atol=1e-5)
+    if tokens is None:
+        tokens = np.arange(s.T)
+    tokens = np.array([t for t in tokens if not near[t]], dtype=np.int32)
+    ref = oracle.moe_forward(lay, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f, tokens=tokens)
+    got = y_to_f64(y)[tokens]
+    err = rel_err(got, ref["y_f64"])
+    assert err <= TOL[s.wdt], f"{s.name}: max|err|/max|ref| = {err:.3e}"
+    return err, int(near.sum())
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_forward_small(name):
+    s = SMALL[name]
+    lay = inputs.make_layer(s, seed=11)
+    _, y, dbg = run_layer(s, lay)
+    check_layer(s, lay, y, dbg)
+
+
+@pytest.mark.parametrize("name", ["decode_bf16", "prefill_bf16", "skew_small"])
+def test_paths_agree(name):
+    """Decode (weight streaming) and prefill (tcgen05 grouped GEMM) paths give
+    the same routing and outputs within rounding on the same inputs."""
+    s = SMALL[name]
+    lay = inputs.make_layer(s, seed=12)
+    _, y_dec, dbg_dec = run_layer(s, lay, path=moe.PATH_DECODE)
+    layer_pre, y_pre, dbg_pre = run_layer(s, lay, path=moe.PATH_PREFILL)
+    for key in ("topk_idx", "counts", "offsets", "row_token", "assign_row"):
+        assert np.array_equal(dbg_dec[key], dbg_pre[key]), key
+    check_layer(s, lay, y_dec, dbg_dec)
+    check_layer(s, lay, y_pre, dbg_pre)
+    assert rel_err(y_to_f64(y_pre), y_to_f64(y_dec)) <= TOL[s.wdt]
+
+
+def test_deterministic_and_host_api():
+    s = SMALL["int4"]
+    lay = inputs.make_layer(s, seed=13)
+    dev = cuda_layer(lay)
+    layer = make_handle(s, dev)
+    y1 = layer(dev["x"]).clone()
+    y2 = layer(dev["x"]).clone()
+    assert torch.equal(y1, y2)
+    xh = lay["x"].pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    layer.forward_host(xh, yh)
+    assert torch.equal(yh, y1.cpu())
+
+
+FULL_SAMPLE = {"tiny_fp32": None, "mixtral_decode": None, "mixtral_prefill": 6,
+               "fine_int4": 10, "skewed": 32}
+
+
+@pytest.mark.parametrize("name", list(FULL_SAMPLE))
+def test_full_config(name):
+    """The configurations at full size: routing and dispatch for every token,
+    outputs for every token (small) or for a seeded sample of tokens."""
+    s = inputs.CONFIGS[name]
+    lay = inputs.make_layer(s, seed=0)
+    layer, y, dbg = run_layer(s, lay)
+    n = FULL_SAMPLE[name]
+    tokens = None
+    if n is not None:
+        g = np.random.default_rng(0)
+        tokens = np.unique(np.concatenate([[0, s.T - 1], g.choice(s.T, n - 2, replace=False)]))
+    err, near = check_layer(s, lay, y, dbg, tokens)
+    print(f"{name}: path={layer.path_for(s.T)} rel_err={err:.3e} near_ties={near}")
+
+
+# ---------------------------------------------------------------- stages
+def _stage_layer(s, seed):
+    lay = inputs.make_layer(s, seed=seed)
+    return lay, cuda_layer(lay)
+
+
+@pytest.mark.parametrize("E,k,act,bias", [(8, 2, "bf16", False), (32, 4, "f32", True),
+                                          (64, 4, "bf16", True), (256, 8, "bf16", False),
+                                          (200, 7, "f32", False)])
+def test_stage_route_topk(E, k, act, bias):
+    s = S("route", T=77, d=320, E=E, k=k, f=64, act=act, wdt=act,
+          bias="zipf" if bias else "none")
+    lay, dev = _stage_layer(s, 21)
+    T, d = s.T, s.d
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    gap = torch.empty(T, dtype=torch.float32, device="cuda")
+    nb = moe.coli_route_scratch_bytes(T, d, E)
+    scratch = torch.empty(max(nb, 1), dtype=torch.uint8, device="cuda")
+    rc = moe.coli_route_topk(dev["x"], dev["w_router"], dev["b_router"], T, d, E, k, s.act_code,
+                             idx, w, gap, scratch, nb)
+    assert rc == 0, moe.last_error()
+    r_idx, r_w, r_gap, r_inner = oracle_routing(s, lay)
+    near = check_routing(idx.cpu().numpy(), w.cpu().numpy(), r_idx, r_w, r_gap, r_inner)
+    g = gap.cpu().numpy()
+    fin = ~near & np.isfinite(r_gap)
+    assert np.allclose(g[fin], r_gap[fin], rtol=0, atol=1e-5)
+
+
+@pytest.mark.parametrize("T,E,k,act", [(37, 8, 2, "bf16"), (300, 64, 4, "f32"),
+                                       (5000, 64, 4, "bf16"), (3000, 256, 8, "bf16"),
+                                       (1, 1, 1, "bf16")])
+def test_stage_permute(T, E, k, act):
+    d = 128
+    idx = inputs.random_assignments(T, E, k, seed=T).cuda()
+    x = inputs.random_rows(T, d, inputs.DTYPE_CODE[act], seed=3).cuda()
+    n = T * k
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    row_token = torch.empty(n, dtype=torch.int32, device="cuda")
+    assign_row = torch.empty(n, dtype=torch.int32, device="cuda")
+    x_perm = torch.empty(n, d, dtype=x.dtype, device="cuda")
+    nb = moe.coli_permute_scratch_bytes(T, k, E)
+    scratch = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
+    rc = moe.coli_permute(idx, x, T, d, E, k, inputs.DTYPE_CODE[act], counts, offsets, row_token,
+                          assign_row, x_perm, scratch, nb)
+    assert rc == 0, moe.last_error()
+    c, o, rt, ar = oracle.dispatch(idx.cpu().numpy(), E)
+    assert np.array_equal(counts.cpu().numpy(), c)
+    assert np.array_equal(offsets.cpu().numpy(), o)
+    assert np.array_equal(row_token.cpu().numpy(), rt)
+    assert np.array_equal(assign_row.cpu().numpy(), ar)
+    assert torch.equal(x_perm.cpu(), x.cpu()[torch.from_numpy(rt).long()])
+    assert moe.coli_device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["decode_bf16", "int4", "tiny_fp32"])
+def test_stage_expert_ffn(name):
+    s = SMALL[name]
+    lay, dev = _stage_layer(s, 31)
+    layer = make_handle(s, dev)
+    g = np.random.default_rng(5)
+    counts = g.multinomial(s.T * s.k, np.ones(s.E) / s.E)
+    counts[0] = 0  # an empty expert
+    n = int(counts.sum())
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    xp = inputs.random_rows(n, s.d, s.act_code, seed=6)
+    y = torch.empty(n, s.d, dtype=torch.float32, device="cuda")
+    rc = moe.coli_expert_ffn(layer.h, xp.cuda(), torch.from_numpy(offsets).cuda(), n, y)
+    assert rc == 0, moe.last_error()
+    got = y.cpu().numpy().astype(np.float64)
+    ref = np.zeros_like(got)
+    for e in range(s.E):
+        a, b = offsets[e], offsets[e + 1]
+        if b > a:
+            ref[a:b] = oracle.expert_ffn(xp[a:b], s.act_code, lay, e, s.d, s.f, s.w_code)
+    assert rel_err(got, ref) <= TOL[s.wdt]
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_stage_combine(out):
+    T, k, d = 45, 3, 256
+    y_perm = inputs.random_rows(T * k, d, inputs.F32, seed=8)
+    perm = torch.from_numpy(np.random.default_rng(9).permutation(T * k).astype(np.int32))
+    w = inputs.random_gates(T, k, seed=10)
+    code = inputs.DTYPE_CODE[out]
+    y = torch.empty(T, d, dtype=torch.float32 if out == "f32" else torch.bfloat16, device="cuda")
+    rc = moe.coli_combine(y_perm.cuda(), perm.cuda(), w.cuda(), T, k, d, code, y)
+    assert rc == 0, moe.last_error()
+    y64, yo = oracle.combine(y_perm, perm, w, T, k, d, code)
+    if out == "f32":
+        assert rel_err(y.cpu().numpy(), y64) <= 1e-6
+    else:
+        # bf16 outputs: at most one unit in the last place from the oracle's rounding
+        got = y.cpu().view(torch.int16).numpy().astype(np.int32)
+        ref = yo.view(np.int16).astype(np.int32)
+        assert np.max(np.abs(got - ref)) <= 1
