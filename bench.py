@@ -42,6 +42,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="budget of the oracle CPU-baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--experts", type=int, default=0,
+                   help="profiling aid: keep the per-expert shapes but use this many experts "
+                        "(and T scaled to keep the rows per expert)")
     return p.parse_args()
 
 
@@ -221,12 +224,17 @@ def run_coli(args):
     torch.cuda.set_device(local)
     moe.build()
     s = inputs.CONFIGS[args.config]
+    if args.experts:
+        s = s.with_(name=f"{s.name}[E={args.experts}]", E=args.experts,
+                    T=max(1, s.T * args.experts // s.E), k=min(s.k, args.experts))
     host = inputs.make_layer(s, seed=0)
     if rank > 0:  # replicas: same weights, this rank's own tokens
         host["x"] = inputs.random_rows(s.T, s.d, s.act_code, seed=1000 + rank)
     dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in host.items()}
     layer = moe.MoELayer(s.d, s.f, s.E, s.k, s.T, s.act_code, s.w_code, dev)
     x = dev["x"]
+    dev = None  # the handle holds its own copy of the weights
+    torch.cuda.empty_cache()
     y = torch.empty_like(x)
     stream = torch.cuda.current_stream()
     path = {moe.PATH_DECODE: "decode", moe.PATH_PREFILL: "prefill"}[layer.path_for(s.T)]

@@ -74,8 +74,8 @@ namespace {
 
 constexpr int kStages = 5;
 constexpr int kTimingRing = 256;
-constexpr int kSplitRowsCap = 1024;  // split-reduction buffer rows
-constexpr int kMaxSplits = 8;
+constexpr int kSplitRows = 8192;  // rows x slices the split-reduction buffer holds
+constexpr int kMaxSplits = 32;
 
 struct TimingSet {
   cudaEvent_t ev[kStages + 1];
@@ -240,11 +240,12 @@ int run_ffn(coli_moe* h, const void* x_perm, const int32_t* offsets, int n_rows,
                              static_cast<__nv_bfloat16*>(h->H), h->dec_grid, st));
   timing_mark(h, ts, 3, st);
   const int steps = c.weight_dtype == COLI_I4G128 ? f / 128 : f / 32;
-  int splits = dec_down_splits(n_rows, E, d, steps, h->dec_grid * 8);
-  if (n_rows > kSplitRowsCap) splits = 1;
+  int max_splits = kSplitRows / n_rows;
+  if (max_splits > kMaxSplits) max_splits = kMaxSplits;
+  const int splits = dec_down_splits(n_rows, E, d, steps, h->dec_grid * 8, max_splits);
   if (splits > 1) {
     CUDA_TRY(launch_dec_down(h->w, static_cast<const __nv_bfloat16*>(h->H), offsets, E, d, f,
-                             splits, h->y_part, static_cast<size_t>(kSplitRowsCap) * d,
+                             splits, h->y_part, static_cast<size_t>(n_rows) * d,
                              h->dec_grid, st));
   } else {
     CUDA_TRY(launch_dec_down(h->w, static_cast<const __nv_bfloat16*>(h->H), offsets, E, d, f, 1,
@@ -350,8 +351,7 @@ int coli_moe_create(const coli_moe_config* cfg, const coli_moe_weights* wts, voi
       {&h->x_perm, Na * d * asz},
       {&h->H, Na * f * static_cast<size_t>(hsz)},
       {reinterpret_cast<void**>(&h->y_perm), Na * d * sizeof(float)},
-      {reinterpret_cast<void**>(&h->y_part),
-       static_cast<size_t>(kMaxSplits) * kSplitRowsCap * d * sizeof(float)},
+      {reinterpret_cast<void**>(&h->y_part), static_cast<size_t>(kSplitRows) * d * sizeof(float)},
       {&h->route_scratch, route_scratch_bytes(static_cast<int>(Tm), d, E)},
       {&h->perm_scratch, permute_scratch_bytes(static_cast<int>(Tm), k, E)},
       {&h->x_stage, Tm * d * asz},
@@ -425,7 +425,7 @@ int coli_moe_forward(coli_moe* h, const void* x, int32_t T, void* y, void* strea
                    err, err_len);
   if (rc) return rc;
   const float* part = splits > 1 ? h->y_part : h->y_perm;
-  CUDA_TRY(launch_combine(part, splits, static_cast<size_t>(kSplitRowsCap) * d, h->assign_row,
+  CUDA_TRY(launch_combine(part, splits, static_cast<size_t>(n_rows) * d, h->assign_row,
                           h->topk_w, T, k, d, c.act_dtype, y, st));
   launches += 1;
   timing_mark(h, ts, 5, st);
@@ -603,7 +603,7 @@ int coli_expert_ffn(const coli_moe* hc, const void* x_perm, const int32_t* offse
                    err_len);
   if (rc) return rc;
   if (splits > 1)
-    CUDA_TRY(launch_reduce_splits(h->y_part, splits, static_cast<size_t>(kSplitRowsCap) * h->cfg.d_model,
+    CUDA_TRY(launch_reduce_splits(h->y_part, splits, static_cast<size_t>(n_rows) * h->cfg.d_model,
                                   n_rows, h->cfg.d_model, y_perm, st));
   return COLI_OK;
 }

@@ -42,7 +42,7 @@ struct FfnWeights {
 
 // Tensor-core decode path: streams the weights of every non-empty expert once.
 // steps = reduction steps of one down row (f/32 bf16, f/128 int4)
-int dec_down_splits(int n_rows, int E, int d, int steps, int n_warps);
+int dec_down_splits(int n_rows, int E, int d, int steps, int n_warps, int max_splits);
 cudaError_t launch_dec_gateup(const FfnWeights& w, const __nv_bfloat16* x_perm,
                               const int32_t* offsets, int E, int d, int f, __nv_bfloat16* H,
                               int grid, cudaStream_t st);

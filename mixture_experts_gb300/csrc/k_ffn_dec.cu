@@ -354,14 +354,30 @@ int dec_blocks_per_sm() {
   return c < 1 ? 1 : c;
 }
 
-int dec_down_splits(int n_rows, int E, int d, int steps, int n_warps) {
+int dec_down_splits(int n_rows, int E, int d, int steps, int n_warps, int max_splits) {
+  // Items (expert, 32 outputs, slice) are dealt round-robin to the warps, so
+  // the slowest warp does ceil(items / warps) of them: pick the fewest
+  // slices that keep that within 5% of the mean (or the best balance), with
+  // at least 8 reduction steps per slice.
   const int active = n_rows < E ? n_rows : E;  // at most this many non-empty experts
-  if (active <= 0) return 1;
-  const long items = static_cast<long>(active) * (d / 32);
-  long s = (2L * n_warps + items - 1) / items;
-  if (s > 8) s = 8;
-  if (s > steps) s = steps;
-  return s < 1 ? 1 : static_cast<int>(s);
+  if (active <= 0 || max_splits <= 1) return 1;
+  const long per = static_cast<long>(active) * (d / 32);
+  int best = 1;
+  double best_eff = 0.0;
+  for (int s = 1; s <= max_splits && steps / s >= 8; ++s) {
+    const long items = per * s;
+    if (items < n_warps && s < max_splits) {
+      // fewer items than warps: every extra slice adds parallelism
+      const double eff = static_cast<double>(items) / n_warps;
+      if (eff > best_eff) { best_eff = eff; best = s; }
+      continue;
+    }
+    const long rounds = (items + n_warps - 1) / n_warps;
+    const double eff = static_cast<double>(items) / (static_cast<double>(rounds) * n_warps);
+    if (eff >= 0.95) return s;
+    if (eff > best_eff + 1e-9) { best_eff = eff; best = s; }
+  }
+  return best;
 }
 
 cudaError_t launch_dec_gateup(const FfnWeights& w, const __nv_bfloat16* x_perm,

@@ -18,32 +18,35 @@ __global__ void __launch_bounds__(256)
     k_combine(const float* __restrict__ part, int splits, size_t part_stride,
               const int32_t* __restrict__ assign_row, const float* __restrict__ topk_w, int T,
               int k, int d, void* __restrict__ y) {
+  // block (token t, 1024-wide column slab); one float4 column per thread
   const int t = blockIdx.x;
   const int d4 = d / 4;
-  for (int c = threadIdx.x; c < d4; c += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const size_t a = static_cast<size_t>(t) * k + j;
-      const float g = topk_w[a];
-      const size_t base = static_cast<size_t>(assign_row[a]) * d4 + c;
-      float4 v = reinterpret_cast<const float4*>(part)[base];
-      for (int s = 1; s < splits; ++s) {
-        const float4 w = reinterpret_cast<const float4*>(part + s * part_stride)[base];
-        v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
-      }
-      acc.x = fmaf(g, v.x, acc.x);
-      acc.y = fmaf(g, v.y, acc.y);
-      acc.z = fmaf(g, v.z, acc.z);
-      acc.w = fmaf(g, v.w, acc.w);
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;
+  if (c >= d4) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+  for (int j = 0; j < k; ++j) {
+    const size_t a = static_cast<size_t>(t) * k + j;
+    const float g = topk_w[a];
+    const size_t base = static_cast<size_t>(assign_row[a]) * d4 + c;
+    float4 v = reinterpret_cast<const float4*>(part)[base];
+#pragma unroll 4
+    for (int s = 1; s < splits; ++s) {
+      const float4 w = reinterpret_cast<const float4*>(part + s * part_stride)[base];
+      v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
     }
-    if (BF16_OUT) {
-      uint2 o;
-      o.x = pack_bf16x2(acc.x, acc.y);
-      o.y = pack_bf16x2(acc.z, acc.w);
-      reinterpret_cast<uint2*>(y)[static_cast<size_t>(t) * d4 + c] = o;
-    } else {
-      reinterpret_cast<float4*>(y)[static_cast<size_t>(t) * d4 + c] = acc;
-    }
+    acc.x = fmaf(g, v.x, acc.x);
+    acc.y = fmaf(g, v.y, acc.y);
+    acc.z = fmaf(g, v.z, acc.z);
+    acc.w = fmaf(g, v.w, acc.w);
+  }
+  if (BF16_OUT) {
+    uint2 o;
+    o.x = pack_bf16x2(acc.x, acc.y);
+    o.y = pack_bf16x2(acc.z, acc.w);
+    reinterpret_cast<uint2*>(y)[static_cast<size_t>(t) * d4 + c] = o;
+  } else {
+    reinterpret_cast<float4*>(y)[static_cast<size_t>(t) * d4 + c] = acc;
   }
 }
 
@@ -237,13 +240,15 @@ cudaError_t launch_combine(const float* y_part, int splits, size_t part_stride,
                            const int32_t* assign_row, const float* topk_w, int T, int k, int d,
                            int out_dt, void* y, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  const int threads = d / 4 >= 256 ? 256 : ((d / 4 + 31) / 32) * 32;
+  const int d4 = d / 4;
+  const int threads = d4 >= 256 ? 256 : ((d4 + 31) / 32) * 32;
+  const dim3 grid(T, (d4 + threads - 1) / threads);
   if (out_dt == DT_BF16)
-    k_combine<true><<<T, threads, 0, st>>>(y_part, splits, part_stride, assign_row, topk_w, T, k,
-                                           d, y);
+    k_combine<true><<<grid, threads, 0, st>>>(y_part, splits, part_stride, assign_row, topk_w,
+                                              T, k, d, y);
   else
-    k_combine<false><<<T, threads, 0, st>>>(y_part, splits, part_stride, assign_row, topk_w, T,
-                                            k, d, y);
+    k_combine<false><<<grid, threads, 0, st>>>(y_part, splits, part_stride, assign_row, topk_w,
+                                               T, k, d, y);
   return cudaGetLastError();
 }
 

@@ -5,10 +5,12 @@
 // (overview page trdm.cn, section 2.1 "Top-k Selection"); the router hands on
 // only k ids and k scores per token (discosf.com page, section 2.1).
 //
-// E <= 32: one fused kernel, one warp per token. Lanes split the reduction
-// index, every lane ends with all E logits in registers (xor-butterfly sums
-// are bitwise identical in every lane), and lane e ranks expert e against
-// the others: rank(e) = #{e' : l[e'] > l[e] or (l[e'] == l[e] and e' < e)}.
+// E <= 32: one fused kernel, one block per token. Its warps split the
+// reduction index (a single warp per token leaves the GPU latency-bound at
+// decode batch sizes), the partial sums meet in shared memory in fixed warp
+// order, and the selection runs warp-per-token: lane e holds the logit of
+// expert e in a register and ranks it against the others,
+// rank(e) = #{e' : l[e'] > l[e] or (l[e'] == l[e] and e' < e)}.
 // E > 32: logits are too many for one warp's registers and W_r too large to
 // re-read per token, so a tiled fp32 kernel first writes partial dot products
 // over token x expert x reduction-slice tiles (fixed slice order, no atomics),
@@ -58,14 +60,16 @@ __global__ void __launch_bounds__(kWarps * 32)
     k_route_fused(const TA* __restrict__ x, const TA* __restrict__ w, const float* __restrict__ b,
                   int T, int d, int E, int k, int32_t* __restrict__ topk_idx,
                   float* __restrict__ topk_w, float* __restrict__ gap) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  if (t >= T) return;
+  // one block per token: the 8 warps take interleaved 8-wide slices of the
+  // reduction index, then warp 0 adds the 8 partial sums in warp order
+  __shared__ float part[kWarps][EMAX];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x;
   float acc[EMAX];
 #pragma unroll
   for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
   const TA* xr = x + static_cast<size_t>(t) * d;
-  for (int i = lane * 8; i < d; i += 256) {
+  for (int i = (warp * 32 + lane) * 8; i < d; i += kWarps * 256) {
     float xv[8];
     load8(xr + i, xv);
 #pragma unroll
@@ -82,18 +86,27 @@ __global__ void __launch_bounds__(kWarps * 32)
   for (int e = 0; e < EMAX; ++e) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
-    if (e < E && b != nullptr) acc[e] += b[e];
   }
+  if (lane == 0) {
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) part[warp][e] = acc[e];
+  }
+  __syncthreads();
+  if (warp != 0) return;
   // lane e owns expert e
-  float le = -INFINITY;
-#pragma unroll
-  for (int e = 0; e < EMAX; ++e)
-    if (e == lane) le = acc[e];
-  int rank = 0;
-#pragma unroll
-  for (int e = 0; e < EMAX; ++e)
-    if (e < E && beats(acc[e], e, le, lane)) ++rank;
   const bool mine = lane < E;
+  float le = -INFINITY;
+  if (mine) {
+    float v = 0.f;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) v += part[i][lane];
+    le = (b != nullptr) ? v + b[lane] : v;
+  }
+  int rank = 0;
+  for (int e = 0; e < E; ++e) {
+    const float o = __shfl_sync(0xffffffffu, le, e);
+    if (beats(o, e, le, lane)) ++rank;
+  }
   if (!mine) rank = 1 << 20;
   const float m = from_rank(rank, le, 0);
   const bool sel = mine && rank < k;
@@ -253,7 +266,7 @@ cudaError_t launch_route(const void* x, const void* w_r, const float* b_r, int T
   const dim3 grid((T + kWarps - 1) / kWarps);
   if (E <= 32) {
 #define COLI_ROUTE_FUSED(TA, EM)                                                             \
-  k_route_fused<TA, EM><<<grid, block, 0, st>>>(static_cast<const TA*>(x),                 \
+  k_route_fused<TA, EM><<<T, block, 0, st>>>(static_cast<const TA*>(x),                 \
                                                static_cast<const TA*>(w_r), b_r, T, d, E, k, \
                                                topk_idx, topk_w, gap)
     if (act == DT_F32) {
