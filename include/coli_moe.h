@@ -210,6 +210,25 @@ int coli_expert_ffn(const coli_moe* h, const void* x_perm, const int32_t* offset
 int coli_combine(const float* y_perm, const int32_t* assign_row, const float* topk_w,
                  int32_t T, int32_t k, int32_t d, int32_t out, void* y, void* stream);
 
+/* Dispatch without caller scratch, for callers that cannot allocate device
+ * memory where they call it (a plugin inside a host program that owns the
+ * device memory pool, a real-time loop that may not allocate after start-up).
+ * The pages have no counterpart: it is an addition of this library.
+ * Same inputs, outputs and results as coli_permute, but the scratch table
+ * lives in a fixed COLI_PERMUTE_STATIC_SCRATCH_BYTES area inside the library
+ * that each GPU loading the library holds until the process exits; the call
+ * makes no allocation of any kind. Batches whose table would not fit
+ * (coli_permute_scratch_bytes(T, k, E) > COLI_PERMUTE_STATIC_SCRATCH_BYTES,
+ * i.e. T*k > 524288 at E = 256 or T*k > 2097152 at E = 64) are rejected with
+ * COLI_EINVAL. The first call on a device looks up the area's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture. All
+ * calls share the one area, so calls whose kernels overlap on a GPU (other
+ * streams, other threads) race and must be serialised by the caller. */
+#define COLI_PERMUTE_STATIC_SCRATCH_BYTES 65536
+int coli_permute_noalloc(const int32_t* topk_idx, const void* x, int32_t T, int32_t d,
+                         int32_t E, int32_t k, int32_t act, int32_t* counts, int32_t* offsets,
+                         int32_t* row_token, int32_t* assign_row, void* x_perm, void* stream);
+
 /* ---- fault-handling self-test ------------------------------------------ */
 /* Launches one block that waits on a shared-memory barrier nothing will ever
  * complete, giving up after spin_limit polls: it latches COLI_ETIMEOUT and

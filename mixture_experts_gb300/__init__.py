@@ -21,6 +21,7 @@ STATUS = {0: "COLI_OK", -1: "COLI_EINVAL", -2: "COLI_ENOMEM", -3: "COLI_ECUDA",
           -4: "COLI_EUNSUPPORTED", -5: "COLI_EDEVICE", -6: "COLI_ETIMEOUT"}
 COLI_OK, COLI_EINVAL, COLI_ENOMEM, COLI_ECUDA = 0, -1, -2, -3
 COLI_EUNSUPPORTED, COLI_EDEVICE, COLI_ETIMEOUT = -4, -5, -6
+COLI_PERMUTE_STATIC_SCRATCH_BYTES = 65536
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libcoli_moe.so")
@@ -76,6 +77,8 @@ _SIGS = {
     "coli_expert_ffn": ("I", ["P", "P", "P", "I", "P", "P"]),
     "coli_combine": ("I", ["P", "P", "P", "I", "I", "I", "I", "P", "P"]),
     "coli_selftest_bounded_wait": ("I", ["I", "P"]),
+    "coli_permute_noalloc": ("I", ["P", "P", "I", "I", "I", "I", "I", "P", "P", "P", "P", "P",
+                                   "P"]),
 }
 _CT = {"P": ctypes.c_void_p, "I": ctypes.c_int32, "Z": ctypes.c_size_t, "s": ctypes.c_char_p,
        None: None}
@@ -231,6 +234,16 @@ def coli_moe_stage_times(h):
 
 def coli_moe_destroy(h) -> None:
     lib().coli_moe_destroy(_ptr(h))
+
+
+def coli_permute_noalloc(topk_idx, x, T, d, E, k, act, counts, offsets, row_token, assign_row,
+                         x_perm, stream=None) -> int:
+    """coli_permute without caller scratch, for callers that cannot allocate
+    device memory at the call site; its scratch is a fixed area inside the
+    library (COLI_PERMUTE_STATIC_SCRATCH_BYTES), shared by all calls."""
+    return lib().coli_permute_noalloc(_ptr(topk_idx), _ptr(x), T, d, E, k, act, _ptr(counts),
+                                      _ptr(offsets), _ptr(row_token), _ptr(assign_row),
+                                      _ptr(x_perm), _stream(stream))
 
 
 def coli_selftest_bounded_wait(spin_limit: int, stream=None) -> int:

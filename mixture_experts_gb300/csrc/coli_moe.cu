@@ -56,6 +56,8 @@ size_t act_size(int dt) { return dt == COLI_F32 ? 4 : 2; }
 static __device__ int g_device_status;
 
 namespace coli {
+int record_error(int code, const char* msg) { return fail(nullptr, 0, code, "%s", msg); }
+
 int* device_status_ptr() {
   static std::mutex mu;
   static int* ptrs[128] = {};

@@ -10,6 +10,9 @@ namespace coli {
 
 enum { DT_F32 = 0, DT_BF16 = 1, DT_I4G128 = 2 };
 
+// Stores msg as the calling thread's coli_last_error() text; returns code.
+int record_error(int code, const char* msg);
+
 // Per-device status word (first device-side error wins).
 int* device_status_ptr();  // nullptr if the symbol address cannot be taken
 
