@@ -1,27 +1,440 @@
-// A3, prefill path: TMA + tcgen05/TMEM grouped GEMM (placeholder until the
-// kernel lands; tc_supported() reports false so the decode kernels run).
+// A3, prefill path: grouped expert GEMM on the 5th-generation tensor cores.
+//
+// For groups of hundreds of rows per expert the FFN is a dense contraction
+// (per expert: rows x d x 2f for gate/up, rows x f x d for down), so it runs
+// on tcgen05: TMA copies 128x64 activation tiles and 256x64 weight tiles
+// (128-byte swizzle) into a 4-stage shared-memory ring, one thread issues
+// tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32 accumulate) into a tensor
+// memory accumulator, and four epilogue warps read the accumulator back with
+// tcgen05.ld. The accumulator is double-buffered in TMEM (2 x 256 of the 512
+// columns) so the epilogue of one tile overlaps the main loop of the next.
+//
+// Grouping (the per-expert GEMM fed by the token-to-expert map and expert
+// offsets of the trdm.cn overview page, section 3.3): each CTA derives the
+// tile list from the device-side offsets — expert e contributes
+// ceil(rows_e / 128) row tiles x (N / 256) column tiles, experts without rows
+// contribute none (their weights are never read: wzjinhao.cn page,
+// section 2.3) — and walks it with a static stride of gridDim.x, consecutive
+// tiles sharing the weight tile so the L2 serves the other row tiles. Row
+// tiles that run past an expert's rows are computed but not stored; rows past
+// the last group are zero-filled by TMA.
+//
+// Gate/up epilogue: the weights are interleaved in 64-row blocks (gate rows,
+// then the matching up rows), so accumulator columns c and c + 64 of each
+// 128-column half are gate and up of the same feature; h = silu(gate) * up is
+// written as bf16. Down epilogue: fp32 rows of y_perm.
+//
+// Every mbarrier wait is bounded by one kernel-wide deadline; a CTA that
+// reaches it latches COLI_ETIMEOUT, unwinds all roles, waits briefly for
+// copies in flight, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
 #include "internal.h"
 
 namespace coli {
+namespace {
 
-struct TcPlan {};
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KiB
+constexpr int TMEM_COLS = 512;
+constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA (+TMEM alloc), warps 2-5 epilogue
+constexpr int kMaxE = 256;
 
-bool tc_supported(int, int) { return false; }
+// bf16 x bf16 -> fp32, A and B K-major, M = 128, N = 256.
+constexpr uint32_t kIdesc = (1u << 4)               // D format f32
+                            | (1u << 7)             // A format bf16
+                            | (1u << 10)            // B format bf16
+                            | (uint32_t(BN >> 3) << 17)  // N / 8
+                            | (uint32_t(BM >> 4) << 24); // M / 16
 
-cudaError_t tc_plan_create(TcPlan** plan, const void*, const void*, int, int, int, int) {
+struct __align__(8) Ctrl {
+  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
+  uint32_t tmem_base;
+  int abort;
+  int tile_off[kMaxE + 1];  // first tile of expert e
+  int row_off[kMaxE + 1];   // first row of expert e (the offsets)
+};
+
+constexpr size_t kSmemBytes = 1024 + STAGES * (A_BYTES + B_BYTES) + sizeof(Ctrl);
+
+// ---- PTX wrappers ------------------------------------------------------------------
+COLI_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major tile of 128-byte rows, 128-byte
+// swizzle, 8-row groups 1024 bytes apart.
+COLI_DEV uint64_t sw128_desc(uint32_t addr) {
+  uint64_t d = static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;            // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;    // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;            // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;            // 128-byte swizzle
+  return d;
+}
+
+COLI_DEV void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
+}
+
+COLI_DEV void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+COLI_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+COLI_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+COLI_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Bounded wait against the kernel-wide deadline; also gives up at once when
+// another role has already aborted.
+COLI_DEV bool wait_bar(uint32_t bar, uint32_t parity, uint64_t deadline, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() > deadline) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+struct Tile {
+  int e, nt, mt;
+};
+
+COLI_DEV Tile decode_tile(const Ctrl& C, int E, int n_tiles_n, int t) {
+  int lo = 0, hi = E;  // tile_off[lo] <= t < tile_off[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (C.tile_off[mid] <= t) lo = mid;
+    else hi = mid;
+  }
+  const int rows = C.row_off[lo + 1] - C.row_off[lo];
+  const int mts = (rows + BM - 1) / BM;
+  const int local = t - C.tile_off[lo];
+  return Tile{lo, local / mts, local % mts};
+}
+
+// EPI 0: gate/up + SwiGLU -> bf16 H [rows][N/2]; EPI 1: fp32 out [rows][N].
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tc_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+              const int32_t* __restrict__ offsets, int E, int K, int N, void* __restrict__ out,
+              int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sa = smem_u32(base);
+  const uint32_t sb = sa + STAGES * A_BYTES;
+  Ctrl& C = *reinterpret_cast<Ctrl*>(base + STAGES * (A_BYTES + B_BYTES));
+  volatile int* abort = &C.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t deadline = global_timer_ns() + kWaitTimeoutNs;
+  const int n_tiles_n = (N + BN - 1) / BN;
+  const int kblocks = K / BK;
+
+  // tile table from the expert offsets (warp 0), barriers (thread 0),
+  // tensor memory (warp 1)
+  if (warp == 0) {
+    int mts[kMaxE / 32], sum = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {
+      const int e = lane * (kMaxE / 32) + i;
+      int m = 0;
+      if (e < E) {
+        const int r0 = offsets[e], r1 = offsets[e + 1];
+        C.row_off[e] = r0;
+        if (e == E - 1) C.row_off[E] = r1;
+        m = ((r1 - r0 + BM - 1) / BM) * n_tiles_n;
+      }
+      mts[i] = m;
+      sum += m;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {
+      const int e = lane * (kMaxE / 32) + i;
+      if (e < E) C.tile_off[e] = run;
+      run += mts[i];
+    }
+    if (lane == 31) C.tile_off[E] = incl;  // all tiles
+    if (lane == 0) {
+      for (int s = 0; s < STAGES; ++s) {
+        mbar_init(smem_u32(&C.full[s]), 1);
+        mbar_init(smem_u32(&C.empty[s]), 1);
+      }
+      for (int a = 0; a < 2; ++a) {
+        mbar_init(smem_u32(&C.tfull[a]), 1);
+        mbar_init(smem_u32(&C.tempty[a]), 4);
+      }
+      C.abort = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+  } else if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&C.tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = C.tmem_base;
+  const int total = C.tile_off[E];
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+        const Tile tl = decode_tile(C, E, n_tiles_n, t);
+        const int a_row = C.row_off[tl.e] + tl.mt * BM;
+        const int b_row = tl.e * N + tl.nt * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!wait_bar(smem_u32(&C.empty[stage]), phase ^ 1u, deadline, abort)) break;
+          const uint32_t fb = smem_u32(&C.full[stage]);
+          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
+          tma_load_2d(sa + stage * A_BYTES, &map_a, fb, kb * BK, a_row);
+          tma_load_2d(sb + stage * B_BYTES, &map_b, fb, kb * BK, b_row);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA issuer
+      int stage = 0, local = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!wait_bar(smem_u32(&C.tempty[acc]), acc_phase ^ 1u, deadline, abort)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!wait_bar(smem_u32(&C.full[stage]), phase, deadline, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = sa + stage * A_BYTES, b0 = sb + stage * B_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32),
+                      (kb | k) != 0 ? 1u : 0u);
+          umma_commit(smem_u32(&C.empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&C.tfull[acc]));
+      }
+    }
+  } else {  // ---- epilogue: warps 2..5, TMEM lanes 32*(warp%4) ..
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int local = 0;
+    for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x, ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!wait_bar(smem_u32(&C.tfull[acc]), acc_phase, deadline, abort)) break;
+      tc_fence_after();
+      const Tile tl = decode_tile(C, E, n_tiles_n, t);
+      const int row = C.row_off[tl.e] + tl.mt * BM + r;
+      const bool valid = row < C.row_off[tl.e + 1];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if constexpr (EPI == 0) {
+        const int F = N / 2;  // features
+        __nv_bfloat16* H = static_cast<__nv_bfloat16*>(out);
+#pragma unroll 1
+        for (int ci = 0; ci < 4; ++ci) {
+          const int c = (ci & 1) + (ci >> 1) * 4;  // gate chunks 0, 1, 4, 5
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c * 32, g);
+          tmem_ld32(taddr + (c + 2) * 32, u);
+          const int feat = tl.nt * 128 + (c & 1) * 32 + (c >> 2) * 64;
+          if (valid && feat < F) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float a0 = __uint_as_float(g[2 * j]), a1 = __uint_as_float(g[2 * j + 1]);
+              const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
+              packed[j] = pack_bf16x2(a0 / (1.f + expf(-a0)) * u0, a1 / (1.f + expf(-a1)) * u1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(H + static_cast<size_t>(row) * F + feat);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                  packed[4 * v + 3]);
+          }
+        }
+      } else {
+        float* Y = static_cast<float*>(out);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c * 32, v);
+          const int col = tl.nt * BN + c * 32;
+          if (valid && col < N) {
+            uint4* dst = reinterpret_cast<uint4*>(Y + static_cast<size_t>(row) * N + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&C.tempty[acc]));
+    }
+  }
+
+  __syncthreads();
+  if (*abort) {
+    if (threadIdx.x == 0) {
+      latch_error(status, kErrTimeout);
+      const uint64_t t0 = global_timer_ns();  // let copies in flight land
+      while (global_timer_ns() - t0 < 1000000ull) {
+      }
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 [rows][cols] row-major, box [box_rows][64], 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+struct TcPlan {
+  CUtensorMap map_wgu, map_wdn;
+  int E, d, f, grid;
+};
+
+bool tc_supported(int d, int f) { return d % 64 == 0 && f % 64 == 0 && encode_fn() != nullptr; }
+
+cudaError_t tc_plan_create(TcPlan** plan, const void* w_gu, const void* w_dn, int E, int d, int f,
+                           int max_rows) {
+  (void)max_rows;
   *plan = nullptr;
-  return cudaErrorNotSupported;
+  TcPlan* p = new TcPlan();
+  p->E = E;
+  p->d = d;
+  p->f = f;
+  int dev = 0, sms = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+    delete p;
+    return e;
+  }
+  p->grid = sms;
+  if ((e = make_map(&p->map_wgu, w_gu, static_cast<uint64_t>(E) * 2 * f, d, BN)) !=
+          cudaSuccess ||
+      (e = make_map(&p->map_wdn, w_dn, static_cast<uint64_t>(E) * d, f, BN)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(k_tc_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kSmemBytes))) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(k_tc_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kSmemBytes))) != cudaSuccess) {
+    delete p;
+    return e;
+  }
+  *plan = p;
+  return cudaSuccess;
 }
 
 void tc_plan_destroy(TcPlan* plan) { delete plan; }
 
-cudaError_t launch_tc_gateup(TcPlan*, const void*, const int32_t*, void*, int, cudaStream_t,
-                             int*) {
-  return cudaErrorNotSupported;
+cudaError_t launch_tc_gateup(TcPlan* p, const void* x_perm, const int32_t* offsets, void* H,
+                             int n_rows, cudaStream_t st, int* status) {
+  if (n_rows == 0) return cudaSuccess;
+  CUtensorMap map_a;
+  cudaError_t e = make_map(&map_a, x_perm, static_cast<uint64_t>(n_rows), p->d, BM);
+  if (e != cudaSuccess) return e;
+  k_tc_gemm<0><<<p->grid, kThreads, kSmemBytes, st>>>(map_a, p->map_wgu, offsets, p->E, p->d,
+                                                       2 * p->f, H, status);
+  return cudaGetLastError();
 }
 
-cudaError_t launch_tc_down(TcPlan*, const void*, const int32_t*, float*, int, cudaStream_t, int*) {
-  return cudaErrorNotSupported;
+cudaError_t launch_tc_down(TcPlan* p, const void* H, const int32_t* offsets, float* y_perm,
+                           int n_rows, cudaStream_t st, int* status) {
+  if (n_rows == 0) return cudaSuccess;
+  CUtensorMap map_a;
+  cudaError_t e = make_map(&map_a, H, static_cast<uint64_t>(n_rows), p->f, BM);
+  if (e != cudaSuccess) return e;
+  k_tc_gemm<1><<<p->grid, kThreads, kSmemBytes, st>>>(map_a, p->map_wdn, offsets, p->E, p->f,
+                                                       p->d, y_perm, status);
+  return cudaGetLastError();
 }
 
 }  // namespace coli

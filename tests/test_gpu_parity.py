@@ -75,6 +75,7 @@ def test_paths_agree(name):
     lay = inputs.make_layer(s, seed=12)
     _, y_dec, dbg_dec = run_layer(s, lay, path=moe.PATH_DECODE)
     layer_pre, y_pre, dbg_pre = run_layer(s, lay, path=moe.PATH_PREFILL)
+    assert layer_pre.path_for(s.T) == moe.PATH_PREFILL
     for key in ("topk_idx", "counts", "offsets", "row_token", "assign_row"):
         assert np.array_equal(dbg_dec[key], dbg_pre[key]), key
     check_layer(s, lay, y_dec, dbg_dec)
