@@ -62,6 +62,25 @@ COLI_DEV uint4 ldg_keep(const void* p) {
   return r;
 }
 
+// 16-byte asynchronous global -> shared copy (L1 bypassed, 256-byte L2 fetch),
+// grouped with cp_async_commit and completed with cp_async_wait<N>.
+COLI_DEV void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(dst), "l"(src)
+               : "memory");
+}
+COLI_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+COLI_DEV void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+COLI_DEV uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 // ---- warp-level tensor-core MMA (m16n8k16, bf16 in, fp32 accumulate) --------
 COLI_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                              uint32_t a3, uint32_t b0, uint32_t b1) {

@@ -1,6 +1,7 @@
 // Host-side launchers shared between the translation units of libcoli_moe.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -12,6 +13,12 @@ enum { DT_F32 = 0, DT_BF16 = 1, DT_I4G128 = 2 };
 
 // Stores msg as the calling thread's coli_last_error() text; returns code.
 int record_error(int code, const char* msg);
+
+// 2-D tensor map over a row-major [rows][cols] array (the driver's encoder is
+// fetched at run time, so the library does not link libcuda).
+cudaError_t encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr,
+                           uint64_t rows, uint64_t cols, int box_cols, int box_rows,
+                           CUtensorMapSwizzle swizzle);
 
 // Per-device status word (first device-side error wins).
 int* device_status_ptr();  // nullptr if the symbol address cannot be taken

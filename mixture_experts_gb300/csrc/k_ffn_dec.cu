@@ -43,22 +43,32 @@ constexpr int kWarpsPerBlock = kThreads / 32;
 template <bool INT4>
 constexpr int kMaxRowsPerPass = INT4 ? 16 : 32;  // token rows per weight pass
 
+// int4: per-warp cp.async ring, kRing steps of 4 x 16 bytes per lane
+constexpr int kRing = 4;
+constexpr int kRingStep = 4 * 32 * 16;  // 2 KiB per warp and step
+constexpr size_t kI4Smem = static_cast<size_t>(kThreads / 32) * kRing * kRingStep;
+extern __shared__ __align__(16) uint8_t dec_smem[];
+
 COLI_DEV uint4 zero4() { return make_uint4(0u, 0u, 0u, 0u); }
 
-// Two nibbles (bits 0-3 and 16-19 of w >> 4j) -> bf16x2 integers q.
-COLI_DEV uint32_t nib_pair(uint32_t w, int j) {
-  uint32_t v = w >> (4 * j);
+// int4 -> bf16 without an offset subtraction. A repacked word holds the 8
+// indices 8w..8w+7 with even ones in nibbles 0-3 and odd ones in 4-7, so
+// nibbles (p, p+4) are the consecutive pair (2p, 2p+1). One LOP3 per pair
+// flips the nibble's sign bit and drops it into the low mantissa bits of a
+// bf16 whose exponent makes the value exactly 136 + q:
+//   ((w >> 4p) & 0x000F000F) ^ 0x43084308  ->  bf16x2 (136 + q_2p, 136 + q_2p+1)
+// The MMA thus sums (136 + q) x; the offset 136 * sum(x) is removed with two
+// MMAs against a constant A per 8 indices (see mainloop), which leaves the
+// exact sum q x of the stored weights.
+COLI_DEV uint32_t nib_pair136(uint32_t w, int p) {
   uint32_t r;
-  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(v), "r"(0x000F000Fu), "r"(0x43084308u));
-  // (v & 0x000F000F) ^ 0x43084308  ->  bf16 (136 + q) in each half
-  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&r);
-  const __nv_bfloat162 off = __floats2bfloat162_rn(136.f, 136.f);
-  x = __hsub2(x, off);
-  return *reinterpret_cast<uint32_t*>(&x);
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(w >> (4 * p)), "r"(0x000F000Fu),
+      "r"(0x43084308u));
+  return r;  // (v & mask) ^ x
 }
 
-COLI_DEV uint4 dequant_word(uint32_t w) {
-  return make_uint4(nib_pair(w, 0), nib_pair(w, 1), nib_pair(w, 2), nib_pair(w, 3));
+COLI_DEV uint4 dequant136(uint32_t w) {
+  return make_uint4(nib_pair136(w, 0), nib_pair136(w, 1), nib_pair136(w, 2), nib_pair136(w, 3));
 }
 
 COLI_DEV uint32_t word_of(const uint4& v, int i) {
@@ -123,56 +133,103 @@ COLI_DEV void mainloop(const uint8_t* const (&wrow)[2][2], const __nv_bfloat16* 
       mma_chunk<NT>(acc, ar, ar8, b);
     }
   } else {
-    // a step = one 128-index group; the lane's x fragment is 64 bytes
-    // (32 consecutive indices) at byte offset 256*s + 64*q.
-    constexpr int U = NT == 1 ? 2 : 1;
-    for (int s = s0; s < s1; s += U) {
-      uint4 a[U][2][2];
-      float sc[U][2][2];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int ss = s + u < s1 ? s + u : s;  // clamp; duplicate work is discarded
+    // A step is one 128-index group. Three things keep a warp's step short:
+    //  - weights: the lane's four 16-byte fragments travel through a
+    //    lane-private cp.async ring in shared memory, kRing - 1 steps ahead
+    //    (many bytes in flight without holding registers); chunk j of every
+    //    lane is contiguous, so the 16-byte accesses are conflict-free;
+    //  - activations: the next step's fragments are loaded into registers
+    //    while this step computes, so the L1/L2 latency is hidden;
+    //  - arithmetic: one LOP3 per weight pair (values 136 + q) and two MMAs
+    //    per 8 indices against a constant A that remove 136 * sum(x).
+    // The lane's x fragment is 64 bytes (32 consecutive indices) at byte
+    // offset 256*s + 64*q; the ring is sized to leave most of L1 to it.
+    const int lane = threadIdx.x & 31;
+    constexpr uint32_t kA136 = 0x43084308u;  // bf16x2 (136, 136)
+    const uint32_t ring = smem_u32(dec_smem) + (threadIdx.x >> 5) * kRing * kRingStep + lane * 16;
+    auto issue = [&](int step, int slot) {
+      if (step < s1) {
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            a[u][m][h] = ldg_stream(wrow[m][h] + ss * 64);
-            sc[u][m][h] = __bfloat162float(srow[m][h][ss]);
-          }
+          for (int h = 0; h < 2; ++h)
+            cp_async16(ring + slot * kRingStep + (2 * m + h) * 512, wrow[m][h] + step * 64);
       }
+      cp_async_commit();
+    };
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (s + u >= s1) break;
-        float g[2][NT][4];
+    for (int i = 0; i < kRing - 1; ++i) issue(s0 + i, i);
+    // activations one step ahead when a single token tile leaves room for
+    // the extra registers; with two tiles they are loaded at the step start
+    constexpr bool kAhead = NT == 1;
+    uint4 bx[NT][4];
+    if (kAhead) {
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
+      for (int n = 0; n < NT; ++n)
 #pragma unroll
-          for (int n = 0; n < NT; ++n)
+        for (int v = 0; v < 4; ++v)
+          bx[n][v] = xrow[n] ? ldg_keep(xrow[n] + s0 * 256 + v * 16) : zero4();
+    }
+    int slot = 0;
+    for (int s = s0; s < s1; ++s) {
+      issue(s + kRing - 1, slot == 0 ? kRing - 1 : slot - 1);
+      float sc[2][2];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) g[m][n][c] = 0.f;
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) sc[m][h] = __bfloat162float(srow[m][h][s]);
+      cp_async_wait<kRing - 1>();  // this lane's copies of step s have landed
+      uint4 a[2][2];
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) a[m][h] = lds128(ring + slot * kRingStep + (2 * m + h) * 512);
+      slot = slot + 1 == kRing ? 0 : slot + 1;
+      uint4 cx[NT][4];  // this step's activations
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          uint4 bv[NT];
+          if (kAhead) {  // take them, and request the next step's
+            cx[n][v] = bx[n][v];
+            if (s + 1 < s1)
+              bx[n][v] = xrow[n] ? ldg_keep(xrow[n] + (s + 1) * 256 + v * 16) : zero4();
+          } else {
+            cx[n][v] = xrow[n] ? ldg_keep(xrow[n] + s * 256 + v * 16) : zero4();
+          }
+        }
+      float g[2][NT][4], corr[NT][4];
 #pragma unroll
-          for (int n = 0; n < NT; ++n)
-            bv[n] = xrow[n] ? ldg_keep(xrow[n] + (s + u) * 256 + v * 16) : zero4();
-          const uint4 ar[2] = {dequant_word(word_of(a[u][0][0], v)),
-                               dequant_word(word_of(a[u][1][0], v))};
-          const uint4 ar8[2] = {dequant_word(word_of(a[u][0][1], v)),
-                                dequant_word(word_of(a[u][1][1], v))};
-          mma_chunk<NT>(g, ar, ar8, bv);
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          corr[n][c] = 0.f;
+          g[0][n][c] = g[1][n][c] = 0.f;
         }
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
+      for (int v = 0; v < 4; ++v) {
+        uint4 bv[NT];
 #pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            acc[m][n][0] = fmaf(sc[u][m][0], g[m][n][0], acc[m][n][0]);
-            acc[m][n][1] = fmaf(sc[u][m][0], g[m][n][1], acc[m][n][1]);
-            acc[m][n][2] = fmaf(sc[u][m][1], g[m][n][2], acc[m][n][2]);
-            acc[m][n][3] = fmaf(sc[u][m][1], g[m][n][3], acc[m][n][3]);
-          }
+        for (int n = 0; n < NT; ++n) bv[n] = cx[n][v];
+        const uint4 ar[2] = {dequant136(word_of(a[0][0], v)), dequant136(word_of(a[1][0], v))};
+        const uint4 ar8[2] = {dequant136(word_of(a[0][1], v)), dequant136(word_of(a[1][1], v))};
+        mma_chunk<NT>(g, ar, ar8, bv);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {  // 136 * the 8 x values, once per token tile
+          mma_bf16_16816(corr[n], kA136, kA136, kA136, kA136, bv[n].x, bv[n].y);
+          mma_bf16_16816(corr[n], kA136, kA136, kA136, kA136, bv[n].z, bv[n].w);
+        }
       }
+      // sum q x = sum (136 + q) x - 136 sum x, times the row's scale
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            acc[m][n][c] = fmaf(sc[m][c >> 1], g[m][n][c] - corr[n][c], acc[m][n][c]);
     }
+    cp_async_wait<0>();  // no copy of this lane outlives the chunk
   }
 }
 
@@ -343,11 +400,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_dec_down(const DecArgs A) {
 }  // namespace
 
 int dec_blocks_per_sm() {
+  // the int4 kernels hold their weight ring in dynamic shared memory
+  cudaFuncSetAttribute(k_dec_gateup<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(kI4Smem));
+  cudaFuncSetAttribute(k_dec_down<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(kI4Smem));
   int a = 0, b = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_dec_gateup<false>, kThreads, 0) !=
       cudaSuccess)
     a = 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_dec_gateup<true>, kThreads, 0) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_dec_gateup<true>, kThreads, kI4Smem) !=
       cudaSuccess)
     b = 1;
   int c = a < b ? a : b;
@@ -395,7 +457,7 @@ cudaError_t launch_dec_gateup(const FfnWeights& w, const __nv_bfloat16* x_perm,
   A.d = d;
   A.splits = 1;
   A.H = H;
-  if (w.wdt == DT_I4G128) k_dec_gateup<true><<<grid, kThreads, 0, st>>>(A);
+  if (w.wdt == DT_I4G128) k_dec_gateup<true><<<grid, kThreads, kI4Smem, st>>>(A);
   else k_dec_gateup<false><<<grid, kThreads, 0, st>>>(A);
   return cudaGetLastError();
 }
@@ -416,7 +478,7 @@ cudaError_t launch_dec_down(const FfnWeights& w, const __nv_bfloat16* H, const i
   A.splits = splits;
   A.y_part = y_part;
   A.part_stride = part_stride;
-  if (w.wdt == DT_I4G128) k_dec_down<true><<<grid, kThreads, 0, st>>>(A);
+  if (w.wdt == DT_I4G128) k_dec_down<true><<<grid, kThreads, kI4Smem, st>>>(A);
   else k_dec_down<false><<<grid, kThreads, 0, st>>>(A);
   return cudaGetLastError();
 }

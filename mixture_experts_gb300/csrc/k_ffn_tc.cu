@@ -276,7 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x, ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
-      if (!wait_bar(smem_u32(&C.tfull[acc]), acc_phase, deadline, abort)) break;
+      // warp-uniform verdict: tcgen05.ld below is warp-collective
+      if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&C.tfull[acc]), acc_phase, deadline, abort)))
+        break;
       tc_fence_after();
       const Tile tl = decode_tile(C, E, n_tiles_n, t);
       const int row = C.row_off[tl.e] + tl.mt * BM + r;
@@ -346,7 +348,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+// 2-D bf16 [rows][cols] row-major, box [box_rows][64], 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, int box_rows) {
+  return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, rows, cols, BK, box_rows,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (fn == nullptr) {
     void* p = nullptr;
@@ -359,22 +369,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 [rows][cols] row-major, box [box_rows][64], 128-byte swizzle.
-cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, int box_rows) {
+cudaError_t encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr,
+                           uint64_t rows, uint64_t cols, int box_cols, int box_rows,
+                           CUtensorMapSwizzle swizzle) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (fn == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(box_rows)};
+  const cuuint64_t strides[1] = {cols * static_cast<cuuint64_t>(elem_bytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const CUresult r = fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
-
-}  // namespace
 
 struct TcPlan {
   CUtensorMap map_wgu, map_wdn;
