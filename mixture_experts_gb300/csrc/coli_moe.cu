@@ -128,6 +128,7 @@ struct coli_moe {
   void* perm_scratch = nullptr;
   void* x_stage = nullptr;
   void* y_stage = nullptr;
+  float* xsum = nullptr;  // int4: 136 * group sums of x_perm, then of H
   // timing
   bool timing = false;
   TimingSet ring[kTimingRing];
@@ -238,9 +239,19 @@ int run_ffn(coli_moe* h, const void* x_perm, const int32_t* offsets, int n_rows,
     *launches += 2;
     return COLI_OK;
   }
+  const bool i4 = c.weight_dtype == COLI_I4G128;
+  if (i4) {
+    CUDA_TRY(launch_group_sums(static_cast<const __nv_bfloat16*>(x_perm), n_rows, d, h->xsum, st));
+    *launches += 1;
+  }
   CUDA_TRY(launch_dec_gateup(h->w, static_cast<const __nv_bfloat16*>(x_perm), offsets, E, d, f,
-                             static_cast<__nv_bfloat16*>(h->H), h->dec_grid, st));
+                             static_cast<__nv_bfloat16*>(h->H), i4 ? h->xsum : nullptr,
+                             h->dec_grid, st));
   timing_mark(h, ts, 3, st);
+  if (i4) {
+    CUDA_TRY(launch_group_sums(static_cast<const __nv_bfloat16*>(h->H), n_rows, f, h->xsum, st));
+    *launches += 1;
+  }
   const int steps = c.weight_dtype == COLI_I4G128 ? f / 128 : f / 32;
   int max_splits = kSplitRows / n_rows;
   if (max_splits > kMaxSplits) max_splits = kMaxSplits;
@@ -248,10 +259,10 @@ int run_ffn(coli_moe* h, const void* x_perm, const int32_t* offsets, int n_rows,
   if (splits > 1) {
     CUDA_TRY(launch_dec_down(h->w, static_cast<const __nv_bfloat16*>(h->H), offsets, E, d, f,
                              splits, h->y_part, static_cast<size_t>(n_rows) * d,
-                             h->dec_grid, st));
+                             i4 ? h->xsum : nullptr, h->dec_grid, st));
   } else {
     CUDA_TRY(launch_dec_down(h->w, static_cast<const __nv_bfloat16*>(h->H), offsets, E, d, f, 1,
-                             y_perm, 0, h->dec_grid, st));
+                             y_perm, 0, i4 ? h->xsum : nullptr, h->dec_grid, st));
   }
   timing_mark(h, ts, 4, st);
   *launches += 2;
@@ -357,6 +368,8 @@ int coli_moe_create(const coli_moe_config* cfg, const coli_moe_weights* wts, voi
       {&h->route_scratch, route_scratch_bytes(static_cast<int>(Tm), d, E)},
       {&h->perm_scratch, permute_scratch_bytes(static_cast<int>(Tm), k, E)},
       {&h->x_stage, Tm * d * asz},
+      {reinterpret_cast<void**>(&h->xsum),
+       i4 ? Na * static_cast<size_t>((d > f ? d : f) / 128) * sizeof(float) : 0},
       {&h->y_stage, Tm * d * asz},
   };
   for (auto& a : plan)

@@ -53,12 +53,16 @@ struct FfnWeights {
 // Tensor-core decode path: streams the weights of every non-empty expert once.
 // steps = reduction steps of one down row (f/32 bf16, f/128 int4)
 int dec_down_splits(int n_rows, int E, int d, int steps, int n_warps, int max_splits);
+// int4: xsum / hsum = 136 * the per-128-group sums of the activation rows
+// (launch_group_sums), nullptr for bf16.
 cudaError_t launch_dec_gateup(const FfnWeights& w, const __nv_bfloat16* x_perm,
                               const int32_t* offsets, int E, int d, int f, __nv_bfloat16* H,
-                              int grid, cudaStream_t st);
+                              const float* xsum, int grid, cudaStream_t st);
 cudaError_t launch_dec_down(const FfnWeights& w, const __nv_bfloat16* H, const int32_t* offsets,
                             int E, int d, int f, int splits, float* y_part, size_t part_stride,
-                            int grid, cudaStream_t st);
+                            const float* hsum, int grid, cudaStream_t st);
+cudaError_t launch_group_sums(const __nv_bfloat16* rows, int n_rows, int K, float* out,
+                              cudaStream_t st);
 int dec_blocks_per_sm();
 
 // fp32 CUDA-core path (f32 activations and weights).

@@ -57,9 +57,9 @@ COLI_DEV uint4 zero4() { return make_uint4(0u, 0u, 0u, 0u); }
 // flips the nibble's sign bit and drops it into the low mantissa bits of a
 // bf16 whose exponent makes the value exactly 136 + q:
 //   ((w >> 4p) & 0x000F000F) ^ 0x43084308  ->  bf16x2 (136 + q_2p, 136 + q_2p+1)
-// The MMA thus sums (136 + q) x; the offset 136 * sum(x) is removed with two
-// MMAs against a constant A per 8 indices (see mainloop), which leaves the
-// exact sum q x of the stored weights.
+// The MMA thus sums (136 + q) x; subtracting 136 * sum(x) over the group
+// (a per-token table, see k_group_sums) leaves the exact sum q x of the
+// stored weights.
 COLI_DEV uint32_t nib_pair136(uint32_t w, int p) {
   uint32_t r;
   asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(w >> (4 * p)), "r"(0x000F000Fu),
@@ -97,7 +97,7 @@ COLI_DEV void mma_chunk(float (&acc)[2][NT][4], const uint4 (&ar)[2], const uint
 template <bool INT4, int NT>
 COLI_DEV void mainloop(const uint8_t* const (&wrow)[2][2], const __nv_bfloat16* const (&srow)[2][2],
                        const uint8_t* const (&xrow)[NT], int s0, int s1,
-                       float (&acc)[2][NT][4]) {
+                       float (&acc)[2][NT][4], const float* const (&xs)[NT][2]) {
   if constexpr (!INT4) {
     // loads in flight per lane: U * (4 + NT) x 16 bytes
     constexpr int U = NT == 1 ? 4 : (NT == 2 ? 2 : 1);
@@ -140,12 +140,13 @@ COLI_DEV void mainloop(const uint8_t* const (&wrow)[2][2], const __nv_bfloat16* 
     //    lane is contiguous, so the 16-byte accesses are conflict-free;
     //  - activations: the next step's fragments are loaded into registers
     //    while this step computes, so the L1/L2 latency is hidden;
-    //  - arithmetic: one LOP3 per weight pair (values 136 + q) and two MMAs
-    //    per 8 indices against a constant A that remove 136 * sum(x).
+    //  - arithmetic: one LOP3 per weight pair (values 136 + q); the offset
+    //    136 * sum(x) of each token and group comes from a table made once
+    //    per forward (k_group_sums), so the tensor pipe only does the
+    //    weight MMAs (legacy MMA issue rate is what bounds this loop).
     // The lane's x fragment is 64 bytes (32 consecutive indices) at byte
     // offset 256*s + 64*q; the ring is sized to leave most of L1 to it.
     const int lane = threadIdx.x & 31;
-    constexpr uint32_t kA136 = 0x43084308u;  // bf16x2 (136, 136)
     const uint32_t ring = smem_u32(dec_smem) + (threadIdx.x >> 5) * kRing * kRingStep + lane * 16;
     auto issue = [&](int step, int slot) {
       if (step < s1) {
@@ -198,14 +199,14 @@ COLI_DEV void mainloop(const uint8_t* const (&wrow)[2][2], const __nv_bfloat16* 
             cx[n][v] = xrow[n] ? ldg_keep(xrow[n] + s * 256 + v * 16) : zero4();
           }
         }
-      float g[2][NT][4], corr[NT][4];
+      float g[2][NT][4], corr[NT][2];
 #pragma unroll
-      for (int n = 0; n < NT; ++n)
+      for (int n = 0; n < NT; ++n) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          corr[n][c] = 0.f;
-          g[0][n][c] = g[1][n][c] = 0.f;
-        }
+        for (int c = 0; c < 4; ++c) g[0][n][c] = g[1][n][c] = 0.f;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) corr[n][t] = xs[n][t] ? xs[n][t][s] : 0.f;  // 136 sum x
+      }
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         uint4 bv[NT];
@@ -214,11 +215,6 @@ COLI_DEV void mainloop(const uint8_t* const (&wrow)[2][2], const __nv_bfloat16* 
         const uint4 ar[2] = {dequant136(word_of(a[0][0], v)), dequant136(word_of(a[1][0], v))};
         const uint4 ar8[2] = {dequant136(word_of(a[0][1], v)), dequant136(word_of(a[1][1], v))};
         mma_chunk<NT>(g, ar, ar8, bv);
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {  // 136 * the 8 x values, once per token tile
-          mma_bf16_16816(corr[n], kA136, kA136, kA136, kA136, bv[n].x, bv[n].y);
-          mma_bf16_16816(corr[n], kA136, kA136, kA136, kA136, bv[n].z, bv[n].w);
-        }
       }
       // sum q x = sum (136 + q) x - 136 sum x, times the row's scale
 #pragma unroll
@@ -227,13 +223,14 @@ COLI_DEV void mainloop(const uint8_t* const (&wrow)[2][2], const __nv_bfloat16* 
         for (int n = 0; n < NT; ++n)
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            acc[m][n][c] = fmaf(sc[m][c >> 1], g[m][n][c] - corr[n][c], acc[m][n][c]);
+            acc[m][n][c] = fmaf(sc[m][c >> 1], g[m][n][c] - corr[n][c & 1], acc[m][n][c]);
     }
     cp_async_wait<0>();  // no copy of this lane outlives the chunk
   }
 }
 
 struct DecArgs {
+  const float* xsum;             // int4: 136 * per-group sums of the activation rows
   const uint8_t* w;              // gate/up or down weights (bytes)
   const __nv_bfloat16* s;        // int4 scales or nullptr
   const __nv_bfloat16* x;        // activations [rows][K] (x_perm or H)
@@ -287,7 +284,15 @@ COLI_DEV void gateup_chunk(const DecArgs& A, int e, int n0, int row0, int nrows)
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[m][n][c] = 0.f;
   const int steps = INT4 ? A.K / 128 : A.K / 32;
-  mainloop<INT4, NT>(wrow, srow, xrow, 0, steps, acc);
+  const float* xs[NT][2];
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int j = 8 * n + 2 * q + t;  // the accumulator columns this lane holds
+      xs[n][t] = (INT4 && j < nrows) ? A.xsum + static_cast<size_t>(row0 + j) * gs : nullptr;
+    }
+  mainloop<INT4, NT>(wrow, srow, xrow, 0, steps, acc, xs);
   // acc[0] = gate, acc[1] = up: rows (features) r, r+8; columns (tokens) 2q, 2q+1
 #pragma unroll
   for (int n = 0; n < NT; ++n)
@@ -335,7 +340,15 @@ COLI_DEV void down_chunk(const DecArgs& A, int e, int o0, int split, int row0, i
   const int steps = INT4 ? A.K / 128 : A.K / 32;
   const int s0 = static_cast<int>(static_cast<long>(steps) * split / A.splits);
   const int s1 = static_cast<int>(static_cast<long>(steps) * (split + 1) / A.splits);
-  mainloop<INT4, NT>(wrow, srow, xrow, s0, s1, acc);
+  const float* xs[NT][2];
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int j = 8 * n + 2 * q + t;  // the accumulator columns this lane holds
+      xs[n][t] = (INT4 && j < nrows) ? A.xsum + static_cast<size_t>(row0 + j) * gs : nullptr;
+    }
+  mainloop<INT4, NT>(wrow, srow, xrow, s0, s1, acc, xs);
   float* out = A.y_part + static_cast<size_t>(split) * A.part_stride;
 #pragma unroll
   for (int m = 0; m < 2; ++m)
@@ -397,7 +410,36 @@ __global__ void __launch_bounds__(kThreads, 2) k_dec_down(const DecArgs A) {
   }
 }
 
+// out[r][g] = 136 * sum of the 128 activations of group g of row r (fp32,
+// fixed order: 4 per lane, then a butterfly), one warp per (row, group).
+__global__ void __launch_bounds__(256)
+    k_group_sums(const __nv_bfloat16* __restrict__ rows, int n_rows, int K,
+                 float* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int groups = K / 128;
+  const long total = static_cast<long>(n_rows) * groups;
+  for (long w = blockIdx.x * 8L + (threadIdx.x >> 5); w < total; w += gridDim.x * 8L) {
+    const long r = w / groups;
+    const int g = static_cast<int>(w % groups);
+    const uint2 v = *reinterpret_cast<const uint2*>(rows + r * K + g * 128 + lane * 4);
+    float sum = (bf16_lo(v.x) + bf16_hi(v.x)) + (bf16_lo(v.y) + bf16_hi(v.y));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0) out[w] = 136.f * sum;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_group_sums(const __nv_bfloat16* rows, int n_rows, int K, float* out,
+                              cudaStream_t st) {
+  if (n_rows == 0) return cudaSuccess;
+  const long warps = static_cast<long>(n_rows) * (K / 128);
+  long grid = (warps + 7) / 8;
+  if (grid > 4096) grid = 4096;
+  k_group_sums<<<static_cast<unsigned>(grid), 256, 0, st>>>(rows, n_rows, K, out);
+  return cudaGetLastError();
+}
 
 int dec_blocks_per_sm() {
   // the int4 kernels hold their weight ring in dynamic shared memory
@@ -444,8 +486,9 @@ int dec_down_splits(int n_rows, int E, int d, int steps, int n_warps, int max_sp
 
 cudaError_t launch_dec_gateup(const FfnWeights& w, const __nv_bfloat16* x_perm,
                               const int32_t* offsets, int E, int d, int f, __nv_bfloat16* H,
-                              int grid, cudaStream_t st) {
+                              const float* xsum, int grid, cudaStream_t st) {
   DecArgs A{};
+  A.xsum = xsum;
   A.w = static_cast<const uint8_t*>(w.w_gu);
   A.s = w.s_gu;
   A.x = x_perm;
@@ -464,8 +507,9 @@ cudaError_t launch_dec_gateup(const FfnWeights& w, const __nv_bfloat16* x_perm,
 
 cudaError_t launch_dec_down(const FfnWeights& w, const __nv_bfloat16* H, const int32_t* offsets,
                             int E, int d, int f, int splits, float* y_part, size_t part_stride,
-                            int grid, cudaStream_t st) {
+                            const float* hsum, int grid, cudaStream_t st) {
   DecArgs A{};
+  A.xsum = hsum;
   A.w = static_cast<const uint8_t*>(w.w_dn);
   A.s = w.s_dn;
   A.x = H;
