@@ -12,8 +12,9 @@
 // expert e in a register and ranks it against the others,
 // rank(e) = #{e' : l[e'] > l[e] or (l[e'] == l[e] and e' < e)}.
 // E > 32: logits are too many for one warp's registers and W_r too large to
-// re-read per token, so a tiled fp32 kernel first writes partial dot products
-// over token x expert x reduction-slice tiles (fixed slice order, no atomics),
+// re-read per token, so a tiled kernel (tensor cores for bf16, CUDA cores for
+// fp32) first writes partial dot products over token x expert x
+// reduction-slice tiles (fixed slice order, no atomics),
 // then a warp-per-token kernel sums the slices, keeps E/32 logits per lane in
 // registers and takes k+1 rounds of warp arg-max (larger value, then lower
 // index) for the top-k and the k-th/(k+1)-th gap.
@@ -178,6 +179,71 @@ __global__ void __launch_bounds__(128)
   }
 }
 
+// Tensor-core logits for bf16 inputs: a block of 4 warps takes 16 tokens x
+// 64 experts over one 512-wide reduction slice with mma.sync m16n8k16
+// (tokens are M, experts N; warp w owns experts 16w..16w+15). Four 32-index
+// steps of loads are issued before any is used, so 8 KiB per warp are in
+// flight (the slice is latency-bound otherwise); the four warps read the
+// same token rows, which L1 serves after the first. Products of bf16 values
+// are exact in fp32; to keep the sum at fp32 round-to-nearest accuracy
+// whatever the tensor core's internal adder does, every 32-index step goes
+// into a zeroed accumulator that is added to the running sum with an FADD.
+// Same partial-slice output as k_route_partial.
+constexpr int kTcTok = 16, kTcExp = 64;
+
+__global__ void __launch_bounds__(128)
+    k_route_partial_tc(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,
+                       int T, int d, int E, float* __restrict__ part) {
+  constexpr int U = 4;
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3, warp = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * kTcTok;
+  const int e0 = blockIdx.y * kTcExp + 16 * warp;
+  const int k0 = blockIdx.z * kKS, k1 = min(d, k0 + kKS);
+  const __nv_bfloat16* xr0 = (t0 + g < T) ? x + static_cast<size_t>(t0 + g) * d + q * 8 : nullptr;
+  const __nv_bfloat16* xr8 =
+      (t0 + g + 8 < T) ? x + static_cast<size_t>(t0 + g + 8) * d + q * 8 : nullptr;
+  const __nv_bfloat16* wr[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int e = e0 + 8 * j + g;
+    wr[j] = e < E ? w + static_cast<size_t>(e) * d + q * 8 : nullptr;
+  }
+  float acc[2][4] = {};
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int k = k0; k < k1; k += 32 * U) {
+    uint4 a[U], a8[U], b[U][2];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int kk = k + 32 * u;
+      const bool in = kk < k1;
+      a[u] = (in && xr0) ? *reinterpret_cast<const uint4*>(xr0 + kk) : z;
+      a8[u] = (in && xr8) ? *reinterpret_cast<const uint4*>(xr8 + kk) : z;
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        b[u][j] = (in && wr[j]) ? *reinterpret_cast<const uint4*>(wr[j] + kk) : z;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_bf16_16816(t, a[u].x, a8[u].x, a[u].y, a8[u].y, b[u][j].x, b[u][j].y);
+        mma_bf16_16816(t, a[u].z, a8[u].z, a[u].w, a8[u].w, b[u][j].z, b[u][j].w);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[j][c] += t[c];
+      }
+  }
+  float* dst = part + static_cast<size_t>(blockIdx.z) * T * E;
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int t = t0 + g + ((c & 2) ? 8 : 0);
+      const int e = e0 + 8 * j + 2 * q + (c & 1);
+      if (t < T && e < E) dst[static_cast<size_t>(t) * E + e] = acc[j][c];
+    }
+}
+
 template <int PER_LANE>
 __global__ void __launch_bounds__(kWarps * 32)
     k_route_select(const float* __restrict__ part, int slices, const float* __restrict__ b,
@@ -285,13 +351,15 @@ cudaError_t launch_route(const void* x, const void* w_r, const float* b_r, int T
   float* part = static_cast<float*>(scratch);
   const int S = slices_for(d);
   const dim3 pgrid((T + kTT - 1) / kTT, (E + kTE - 1) / kTE, S);
-  if (act == DT_F32)
+  if (act == DT_F32) {
     k_route_partial<float><<<pgrid, 128, 0, st>>>(static_cast<const float*>(x),
                                                    static_cast<const float*>(w_r), T, d, E, part);
-  else
-    k_route_partial<__nv_bfloat16><<<pgrid, 128, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_r), T, d, E,
-        part);
+  } else {
+    const dim3 tgrid((T + kTcTok - 1) / kTcTok, (E + kTcExp - 1) / kTcExp, S);
+    k_route_partial_tc<<<tgrid, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
+                                               static_cast<const __nv_bfloat16*>(w_r), T, d, E,
+                                               part);
+  }
   if (E <= 64)
     k_route_select<2><<<grid, block, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap);
   else if (E <= 128)

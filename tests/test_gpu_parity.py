@@ -143,7 +143,9 @@ def test_stage_route_topk(E, k, act, bias):
     near = check_routing(idx.cpu().numpy(), w.cpu().numpy(), r_idx, r_w, r_gap, r_inner)
     g = gap.cpu().numpy()
     fin = ~near & np.isfinite(r_gap)
-    assert np.allclose(g[fin], r_gap[fin], rtol=0, atol=1e-5)
+    # a gap is a difference of two fp32 logits: its error bounds the logit
+    # accumulation error (tensor-core path for bf16 with E > 32)
+    assert np.max(np.abs(g[fin] - r_gap[fin]), initial=0.0) <= 3e-6
 
 
 @pytest.mark.parametrize("T,E,k,act", [(37, 8, 2, "bf16"), (300, 64, 4, "f32"),
