@@ -219,7 +219,7 @@ int coli_combine(const float* y_perm, const int32_t* assign_row, const float* to
  * that each GPU loading the library holds until the process exits; the call
  * makes no allocation of any kind. Batches whose table would not fit
  * (coli_permute_scratch_bytes(T, k, E) > COLI_PERMUTE_STATIC_SCRATCH_BYTES,
- * i.e. T*k > 524288 at E = 256 or T*k > 2097152 at E = 64) are rejected with
+ * i.e. T*k > 131072 at E = 256 or T*k > 524288 at E = 64) are rejected with
  * COLI_EINVAL. The first call on a device looks up the area's device address (cudaGetSymbolAddress) with
  * that device current; make that first call before any stream capture. All
  * calls share the one area, so calls whose kernels overlap on a GPU (other

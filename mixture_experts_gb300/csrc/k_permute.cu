@@ -23,7 +23,7 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kFusedMax = 16384;  // assignments handled by the single-block kernel
-constexpr int kChunk = 8192;      // assignments per block in the multi-block kernels
+constexpr int kChunk = 2048;      // assignments per block in the multi-block kernels
 constexpr int kMaxE = 256;
 
 COLI_DEV unsigned lanemask_lt() {

@@ -67,7 +67,7 @@ def test_noalloc_matches_coli_permute_on_two_calls_in_a_row():
 
 
 def test_noalloc_rejects_batches_beyond_its_area():
-    T, k, E = 65537, 8, 256  # needs 65 blocks x 256 experts x 4 bytes > 65536
+    T, k, E = 16385, 8, 256  # needs 65 blocks x 256 experts x 4 bytes > 65536
     assert moe.coli_permute_scratch_bytes(T, k, E) > moe.COLI_PERMUTE_STATIC_SCRATCH_BYTES
     fake = 1 << 20  # never dereferenced: the size check comes first
     rc = moe.coli_permute_noalloc(fake, fake, T, 64, E, k, moe.BF16, fake, fake, fake, fake,
