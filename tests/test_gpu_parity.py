@@ -216,3 +216,40 @@ def test_stage_combine(out):
         got = y.cpu().view(torch.int16).numpy().astype(np.int32)
         ref = yo.view(np.int16).astype(np.int32)
         assert np.max(np.abs(got - ref)) <= 1
+
+
+# ---------------------------------------------------------------- edge cases
+EDGE = {
+    # tensor-core path with a half-filled last column tile (f % 128 == 64) and
+    # a down projection whose last tile runs past d (d % 256 != 0)
+    "tc_tails": S("tc_tails", T=300, d=320, E=4, k=2, f=192),
+    "min_dims": S("min_dims", T=20, d=64, E=3, k=3, f=64),
+    "e256_prefill": S("e256_prefill", T=2048, d=128, E=256, k=8, f=128),
+    "int4_min": S("int4_min", T=12, d=128, E=5, k=2, f=128, wdt="i4g128"),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+@pytest.mark.parametrize("path", [moe.PATH_DECODE, moe.PATH_PREFILL])
+def test_edge_shapes(name, path):
+    s = EDGE[name]
+    lay = inputs.make_layer(s, seed=41)
+    _, y, dbg = run_layer(s, lay, path=path)
+    check_layer(s, lay, y, dbg)
+
+
+def test_empty_batch_is_a_no_op():
+    s = SMALL["decode_bf16"]
+    lay = inputs.make_layer(s, seed=42)
+    dev = cuda_layer(lay)
+    layer = make_handle(s, dev)
+    y = torch.full_like(dev["x"], 7.0)
+    assert moe.coli_moe_forward(layer.h, dev["x"], 0, y) == moe.COLI_OK
+    torch.cuda.synchronize()
+    assert bool((y == 7.0).all())
+    # stage functions accept T == 0 as well
+    z = torch.empty(0, dtype=torch.int32, device="cuda")
+    assert moe.coli_route_topk(dev["x"], dev["w_router"], None, 0, s.d, s.E, s.k, s.act_code,
+                               z, z) == moe.COLI_OK
+    assert moe.coli_combine(dev["x"], z, z, 0, s.k, s.d, s.act_code, y) == moe.COLI_OK
+    assert layer.status() == moe.COLI_OK
