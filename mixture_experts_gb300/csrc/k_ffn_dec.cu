@@ -44,7 +44,7 @@ template <bool INT4>
 constexpr int kMaxRowsPerPass = INT4 ? 16 : 32;  // token rows per weight pass
 
 // int4: per-warp cp.async ring, kRing steps of 4 x 16 bytes per lane
-constexpr int kRing = 4;
+constexpr int kRing = 3;
 constexpr int kRingStep = 4 * 32 * 16;  // 2 KiB per warp and step
 constexpr size_t kI4Smem = static_cast<size_t>(kThreads / 32) * kRing * kRingStep;
 extern __shared__ __align__(16) uint8_t dec_smem[];
