@@ -85,20 +85,45 @@ def aggregate(local_tokens: int, local_seconds: float, world: int):
 
 
 # ---------------------------------------------------------------- CPU oracle leg
+def host_desc() -> str:
+    """CPU model and core count of this host, for the baseline line."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for ln in fh:
+                key = ln.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware") and ":" in ln:
+                    model = ln.split(":", 1)[1].strip()
+                    if key == "model name":
+                        break
+    except OSError:
+        pass
+    return f"1 of {os.cpu_count()} cores ({model or 'unknown CPU'})"
+
+
 def oracle_sample(s, layer, budget_s: float):
-    """Time the oracle (as it stands, one thread) on a bounded sample of this
-    workload's tokens; returns (tokens/s, tokens timed, seconds)."""
+    """Time the oracle (as it stands, one thread pinned to one core) on a
+    bounded sample of this workload's tokens; returns (tokens/s, tokens timed,
+    seconds)."""
     import numpy as np
     import oracle
     oracle.build()
-    t0 = time.perf_counter()
-    oracle.moe_forward(layer, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f, tokens=[0])
-    one = max(time.perf_counter() - t0, 1e-6)
-    n = int(max(1, min(s.T, budget_s / one)))
-    tokens = np.arange(n, dtype=np.int32) % s.T
-    t0 = time.perf_counter()
-    oracle.moe_forward(layer, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f, tokens=tokens)
-    dt = time.perf_counter() - t0
+    saved = None
+    if hasattr(os, "sched_setaffinity"):
+        saved = os.sched_getaffinity(0)
+        os.sched_setaffinity(0, {min(saved)})
+    try:
+        t0 = time.perf_counter()
+        oracle.moe_forward(layer, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f, tokens=[0])
+        one = max(time.perf_counter() - t0, 1e-6)
+        n = int(max(1, min(s.T, budget_s / one)))
+        tokens = np.arange(n, dtype=np.int32) % s.T
+        t0 = time.perf_counter()
+        oracle.moe_forward(layer, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f, tokens=tokens)
+        dt = time.perf_counter() - t0
+    finally:
+        if saved is not None:
+            os.sched_setaffinity(0, saved)
     return n / dt, n, dt
 
 
@@ -128,7 +153,8 @@ def run_reference(args):
         "config": {"workload": workload_desc(s)},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": f"{n_total // max(1, args.steps)} of the {s.T} tokens per "
-                                   f"step, whole layer per token, single thread"},
+                                   f"step, whole layer per token, single thread",
+                         "host": host_desc()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -320,6 +346,13 @@ def run_coli(args):
                 "algorithmic_flops_per_launch": flops,
                 "peak_source": f"{pk_src} bf16_tflops_sustained"}
     ffn_ms = avg[2] + avg[3]
+    # intermediates are not algorithmic bytes: x_perm (written by dispatch,
+    # read by gate/up), H (bf16, written and read), y_perm (fp32, written by
+    # down, read by combine); listed separately per forward
+    asz = 4 if s.act == "f32" else 2
+    roof["overhead_bytes"] = {
+        "x_perm": 2 * n_rows * s.d * asz, "H": 2 * n_rows * s.f * (4 if s.wdt == "f32" else 2),
+        "y_perm": 2 * n_rows * s.d * 4}
     if path == "decode":
         if s.wdt == "i4g128":
             all_bytes = active * (3 * s.f * s.d // 2 + 3 * s.f * (s.d // 128) * 2)
@@ -349,7 +382,8 @@ def run_coli(args):
             tps, n, dt = oracle_sample(s, host, args.cpu_seconds)
             cpu = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                    "sample": f"{n} of the {s.T} tokens of one step, whole layer per token "
-                             f"({dt:.1f} s, one thread)"}
+                             f"({dt:.1f} s, one thread)",
+                   "host": host_desc()}
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,

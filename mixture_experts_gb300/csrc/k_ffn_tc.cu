@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
 
 namespace coli {
 namespace {
@@ -44,11 +45,7 @@ constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA (+TMEM alloc), warps 2-
 constexpr int kMaxE = 256;
 
 // bf16 x bf16 -> fp32, A and B K-major, M = 128, N = 256.
-constexpr uint32_t kIdesc = (1u << 4)               // D format f32
-                            | (1u << 7)             // A format bf16
-                            | (1u << 10)            // B format bf16
-                            | (uint32_t(BN >> 3) << 17)  // N / 8
-                            | (uint32_t(BM >> 4) << 24); // M / 16
+constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
 
 struct __align__(8) Ctrl {
   uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
@@ -59,71 +56,6 @@ struct __align__(8) Ctrl {
 };
 
 constexpr size_t kSmemBytes = 1024 + STAGES * (A_BYTES + B_BYTES) + sizeof(Ctrl);
-
-// ---- PTX wrappers ------------------------------------------------------------------
-COLI_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(map), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major tile of 128-byte rows, 128-byte
-// swizzle, 8-row groups 1024 bytes apart.
-COLI_DEV uint64_t sw128_desc(uint32_t addr) {
-  uint64_t d = static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1) << 16;            // leading byte offset (unused here)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;    // stride byte offset
-  d |= static_cast<uint64_t>(1) << 46;            // descriptor version
-  d |= static_cast<uint64_t>(2) << 61;            // 128-byte swizzle
-  return d;
-}
-
-COLI_DEV void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
-}
-
-COLI_DEV void umma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-COLI_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-COLI_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-COLI_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Bounded wait against the kernel-wide deadline; also gives up at once when
-// another role has already aborted.
-COLI_DEV bool wait_bar(uint32_t bar, uint32_t parity, uint64_t deadline, volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (global_timer_ns() > deadline) {
-      *abort = 1;
-      return false;
-    }
-  }
-}
 
 struct Tile {
   int e, nt, mt;
@@ -204,11 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
   } else if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&C.tmem_base)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tmem_alloc(smem_u32(&C.tmem_base), TMEM_COLS);
   }
   tc_fence_before();
   __syncthreads();
@@ -257,8 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a0 = sa + stage * A_BYTES, b0 = sb + stage * B_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            umma_bf16(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32),
-                      (kb | k) != 0 ? 1u : 0u);
+            umma_ss(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), kIdesc,
+                    (kb | k) != 0 ? 1u : 0u);
           umma_commit(smem_u32(&C.empty[stage]));
           if (++stage == STAGES) {
             stage = 0;
@@ -342,9 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(TMEM_COLS)
-                 : "memory");
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
