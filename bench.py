@@ -98,6 +98,9 @@ def host_desc() -> str:
                         break
     except OSError:
         pass
+    parts = {"0xd4f": "Arm Neoverse-V2", "0xd40": "Arm Neoverse-V1", "0xd0c": "Arm Neoverse-N1"}
+    if model in parts:
+        model = f"{parts[model]}, CPU part {model}"
     return f"1 of {os.cpu_count()} cores ({model or 'unknown CPU'})"
 
 
@@ -221,9 +224,24 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- traffic record
-def traffic_record(config: str, kernel_file: str):
+KERNEL_SOURCES = {
+    "dec": ("k_ffn_dec.cu", "common.cuh"),
+    "tc": ("k_ffn_tc.cu", "tcgen05.cuh", "common.cuh"),
+}
+
+
+def sources_sha(kind: str) -> str:
+    """Hash of the dominant kernel's source files (the .cu and its headers)."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "mixture_experts_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(config: str, kind: str):
     """DRAM bytes per launch of the dominant kernel from a committed ncu
-    summary, if the kernel source is unchanged since the capture."""
+    summary, if the kernel's sources are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -231,9 +249,7 @@ def traffic_record(config: str, kernel_file: str):
         rec = json.load(fh).get(config)
     if not rec:
         return None
-    src = os.path.join(ROOT, "mixture_experts_gb300", "csrc", kernel_file)
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return rec["bytes_per_launch"] if rec.get("source_sha") == sha else None
+    return rec["bytes_per_launch"] if rec.get("source_sha") == sources_sha(kind) else None
 
 
 # ---------------------------------------------------------------- GPU leg
@@ -330,7 +346,7 @@ def run_coli(args):
         achieved = alg / (gu_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"],
-                "traffic": traffic_record(args.config, "k_ffn_dec.cu"),
+                "traffic": traffic_record(args.config, "dec"),
                 "kernel": "k_dec_gateup (expert gate/up projection + SwiGLU)",
                 "algorithmic_bytes_per_launch": alg,
                 "unit_work": f"{per_expert} B of gate/up weights per activated expert x "
@@ -341,7 +357,7 @@ def run_coli(args):
         achieved = flops / (gu_ms / 1e3) / 1e12
         peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic_record(args.config, "k_ffn_tc.cu"),
+                "frac": achieved / peak, "traffic": traffic_record(args.config, "tc"),
                 "kernel": "k_tc_gemm (gate/up grouped GEMM + SwiGLU)",
                 "algorithmic_flops_per_launch": flops,
                 "peak_source": f"{pk_src} bf16_tflops_sustained"}
