@@ -215,7 +215,7 @@ void harvest(coli_moe* h, TimingSet& ts) {
 // through a reduction).
 int run_ffn(coli_moe* h, const void* x_perm, const int32_t* offsets, int n_rows, float* y_perm,
             int T, cudaStream_t st, TimingSet* ts, int* launches, int* splits_out, char* err,
-            size_t err_len) {
+            size_t err_len, const void* x_tok = nullptr, const int32_t* row_token = nullptr) {
   const auto& c = h->cfg;
   const int E = c.n_experts, d = c.d_model, f = c.d_ff;
   int* status = device_status_ptr();
@@ -239,13 +239,17 @@ int run_ffn(coli_moe* h, const void* x_perm, const int32_t* offsets, int n_rows,
     *launches += 2;
     return COLI_OK;
   }
+  // gate/up activations: token rows of x through row_token (no x_perm), or
+  // the caller's permuted rows
   const bool i4 = c.weight_dtype == COLI_I4G128;
+  const void* xa = row_token ? x_tok : x_perm;
+  const int xa_rows = row_token ? T : n_rows;
   if (i4) {
-    CUDA_TRY(launch_group_sums(static_cast<const __nv_bfloat16*>(x_perm), n_rows, d, h->xsum, st));
+    CUDA_TRY(launch_group_sums(static_cast<const __nv_bfloat16*>(xa), xa_rows, d, h->xsum, st));
     *launches += 1;
   }
-  CUDA_TRY(launch_dec_gateup(h->w, static_cast<const __nv_bfloat16*>(x_perm), offsets, E, d, f,
-                             static_cast<__nv_bfloat16*>(h->H), i4 ? h->xsum : nullptr,
+  CUDA_TRY(launch_dec_gateup(h->w, static_cast<const __nv_bfloat16*>(xa), row_token, offsets, E,
+                             d, f, static_cast<__nv_bfloat16*>(h->H), i4 ? h->xsum : nullptr,
                              h->dec_grid, st));
   timing_mark(h, ts, 3, st);
   if (i4) {
@@ -431,13 +435,15 @@ int coli_moe_forward(coli_moe* h, const void* x, int32_t T, void* y, void* strea
   CUDA_TRY(launch_route(x, h->w_router, h->b_router, T, d, E, k, c.act_dtype, h->topk_idx,
                         h->topk_w, h->gap, h->route_scratch, st, &launches));
   timing_mark(h, ts, 1, st);
+  // the decode kernels read token rows of x themselves: no x_perm copy
+  const bool gather = c.weight_dtype != COLI_F32 && pick_path(h, T) == COLI_PATH_DECODE;
   CUDA_TRY(launch_permute(h->topk_idx, x, T, d, E, k, c.act_dtype, h->counts, h->offsets,
-                          h->row_token, h->assign_row, h->x_perm, h->perm_scratch, st, status,
-                          &launches));
+                          h->row_token, h->assign_row, gather ? nullptr : h->x_perm,
+                          h->perm_scratch, st, status, &launches));
   timing_mark(h, ts, 2, st);
   int splits = 1;
   int rc = run_ffn(h, h->x_perm, h->offsets, n_rows, h->y_perm, T, st, ts, &launches, &splits,
-                   err, err_len);
+                   err, err_len, gather ? x : nullptr, gather ? h->row_token : nullptr);
   if (rc) return rc;
   const float* part = splits > 1 ? h->y_part : h->y_perm;
   CUDA_TRY(launch_combine(part, splits, static_cast<size_t>(n_rows) * d, h->assign_row,

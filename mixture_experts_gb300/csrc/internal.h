@@ -54,10 +54,13 @@ struct FfnWeights {
 // steps = reduction steps of one down row (f/32 bf16, f/128 int4)
 int dec_down_splits(int n_rows, int E, int d, int steps, int n_warps, int max_splits);
 // int4: xsum / hsum = 136 * the per-128-group sums of the activation rows
-// (launch_group_sums), nullptr for bf16.
-cudaError_t launch_dec_gateup(const FfnWeights& w, const __nv_bfloat16* x_perm,
-                              const int32_t* offsets, int E, int d, int f, __nv_bfloat16* H,
-                              const float* xsum, int grid, cudaStream_t st);
+// (launch_group_sums), nullptr for bf16. Gate/up activations: row_token
+// nullptr -> x holds the permuted rows (x_perm); otherwise x is [T][d] and
+// row r reads x[row_token[r]] (xsum is then per token too).
+cudaError_t launch_dec_gateup(const FfnWeights& w, const __nv_bfloat16* x,
+                              const int32_t* row_token, const int32_t* offsets, int E, int d,
+                              int f, __nv_bfloat16* H, const float* xsum, int grid,
+                              cudaStream_t st);
 cudaError_t launch_dec_down(const FfnWeights& w, const __nv_bfloat16* H, const int32_t* offsets,
                             int E, int d, int f, int splits, float* y_part, size_t part_stride,
                             const float* hsum, int grid, cudaStream_t st);

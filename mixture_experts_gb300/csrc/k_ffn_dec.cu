@@ -233,7 +233,8 @@ struct DecArgs {
   const float* xsum;             // int4: 136 * per-group sums of the activation rows
   const uint8_t* w;              // gate/up or down weights (bytes)
   const __nv_bfloat16* s;        // int4 scales or nullptr
-  const __nv_bfloat16* x;        // activations [rows][K] (x_perm or H)
+  const __nv_bfloat16* x;        // activations [rows][K] (x_perm or H), or x [T][K]
+  const int32_t* row_token;      // non-null: row r reads x[row_token[r]] (and its xsum row)
   const int32_t* offsets;        // [E+1]
   int E, K;                      // experts, reduction length
   int rows_per_expert;           // weight rows per expert (2f or d)
@@ -268,12 +269,17 @@ COLI_DEV void gateup_chunk(const DecArgs& A, int e, int n0, int row0, int nrows)
       wrow[m][h] = A.w + row * rb + q * 16;
       srow[m][h] = INT4 ? A.s + row * gs : nullptr;
     }
+  // activation row of token column j: the permuted row, or the token's row of
+  // x when the rows are gathered here (the dispatch then copies nothing)
+  auto src_row = [&](int j) -> size_t {
+    return static_cast<size_t>(A.row_token ? A.row_token[row0 + j] : row0 + j);
+  };
   const uint8_t* xrow[NT];
   const int xlane = INT4 ? q * 64 : q * 16;
 #pragma unroll
   for (int n = 0; n < NT; ++n) {
     const int j = 8 * n + r;
-    xrow[n] = j < nrows ? reinterpret_cast<const uint8_t*>(A.x + static_cast<size_t>(row0 + j) * A.K) + xlane
+    xrow[n] = j < nrows ? reinterpret_cast<const uint8_t*>(A.x + src_row(j) * A.K) + xlane
                         : nullptr;
   }
   float acc[2][NT][4];
@@ -290,7 +296,7 @@ COLI_DEV void gateup_chunk(const DecArgs& A, int e, int n0, int row0, int nrows)
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int j = 8 * n + 2 * q + t;  // the accumulator columns this lane holds
-      xs[n][t] = (INT4 && j < nrows) ? A.xsum + static_cast<size_t>(row0 + j) * gs : nullptr;
+      xs[n][t] = (INT4 && j < nrows) ? A.xsum + src_row(j) * gs : nullptr;
     }
   mainloop<INT4, NT>(wrow, srow, xrow, 0, steps, acc, xs);
   // acc[0] = gate, acc[1] = up: rows (features) r, r+8; columns (tokens) 2q, 2q+1
@@ -484,14 +490,16 @@ int dec_down_splits(int n_rows, int E, int d, int steps, int n_warps, int max_sp
   return best;
 }
 
-cudaError_t launch_dec_gateup(const FfnWeights& w, const __nv_bfloat16* x_perm,
-                              const int32_t* offsets, int E, int d, int f, __nv_bfloat16* H,
-                              const float* xsum, int grid, cudaStream_t st) {
+cudaError_t launch_dec_gateup(const FfnWeights& w, const __nv_bfloat16* x,
+                              const int32_t* row_token, const int32_t* offsets, int E, int d,
+                              int f, __nv_bfloat16* H, const float* xsum, int grid,
+                              cudaStream_t st) {
   DecArgs A{};
   A.xsum = xsum;
   A.w = static_cast<const uint8_t*>(w.w_gu);
   A.s = w.s_gu;
-  A.x = x_perm;
+  A.x = x;
+  A.row_token = row_token;
   A.offsets = offsets;
   A.E = E;
   A.K = d;

@@ -70,6 +70,10 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
   for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
   const TA* xr = x + static_cast<size_t>(t) * d;
+  // unrolled so the loads of several slices are in flight at once (less for
+  // many experts, whose accumulators already take the registers)
+  constexpr int kUnroll = EMAX <= 8 ? 4 : (EMAX <= 16 ? 2 : 1);
+#pragma unroll kUnroll
   for (int i = (warp * 32 + lane) * 8; i < d; i += kWarps * 256) {
     float xv[8];
     load8(xr + i, xv);
