@@ -365,9 +365,12 @@ def run_coli(args):
     # intermediates are not algorithmic bytes: x_perm (written by dispatch,
     # read by gate/up), H (bf16, written and read), y_perm (fp32, written by
     # down, read by combine); listed separately per forward
+    # (the decode path with bf16/int4 experts reads token rows of x directly
+    # and writes no x_perm)
     asz = 4 if s.act == "f32" else 2
+    xperm = 0 if (path == "decode" and s.wdt != "f32") else 2 * n_rows * s.d * asz
     roof["overhead_bytes"] = {
-        "x_perm": 2 * n_rows * s.d * asz, "H": 2 * n_rows * s.f * (4 if s.wdt == "f32" else 2),
+        "x_perm": xperm, "H": 2 * n_rows * s.f * (4 if s.wdt == "f32" else 2),
         "y_perm": 2 * n_rows * s.d * 4}
     if path == "decode":
         if s.wdt == "i4g128":
