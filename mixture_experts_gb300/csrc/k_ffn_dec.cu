@@ -253,7 +253,8 @@ COLI_DEV size_t row_bytes(int K) {
 }
 
 template <bool INT4, int NT>
-COLI_DEV void gateup_chunk(const DecArgs& A, int e, int n0, int row0, int nrows) {
+COLI_DEV void gateup_chunk(const DecArgs& A, const int32_t* tok, int e, int n0, int row0,
+                          int nrows) {
   const int lane = threadIdx.x & 31, r = lane >> 2, q = lane & 3;
   const size_t rb = row_bytes<INT4>(A.K);
   const int gs = A.K / 128;
@@ -272,7 +273,7 @@ COLI_DEV void gateup_chunk(const DecArgs& A, int e, int n0, int row0, int nrows)
   // activation row of token column j: the permuted row, or the token's row of
   // x when the rows are gathered here (the dispatch then copies nothing)
   auto src_row = [&](int j) -> size_t {
-    return static_cast<size_t>(A.row_token ? A.row_token[row0 + j] : row0 + j);
+    return static_cast<size_t>(tok ? tok[row0 + j] : row0 + j);
   };
   const uint8_t* xrow[NT];
   const int xlane = INT4 ? q * 64 : q * 16;
@@ -369,24 +370,50 @@ COLI_DEV void down_chunk(const DecArgs& A, int e, int o0, int split, int row0, i
       }
 }
 
+// bf16: the expert offsets (and, for a decode-sized batch, the row -> token
+// map) are copied into shared memory once per block, so no item starts with a
+// dependent global load. Returns the row -> token map to use (the copy, the
+// global one, or nullptr). The int4 kernels declare no static shared memory:
+// their blocks fill the 48 KiB weight ring exactly, and any more would move
+// the SM's shared-memory carve-out up a step and shrink the L1 that holds
+// their activations (measured: 10% slower).
+constexpr int kMaxE = 256;
+constexpr int kTokStage = 2048;
+COLI_DEV const int32_t* stage_maps(const DecArgs& A, int* s_off, int* s_tok) {
+  for (int i = threadIdx.x; i <= A.E; i += blockDim.x) s_off[i] = A.offsets[i];
+  const int n_rows = A.offsets[A.E];
+  const bool tok = s_tok != nullptr && A.row_token != nullptr && n_rows <= kTokStage;
+  if (tok)
+    for (int i = threadIdx.x; i < n_rows; i += blockDim.x) s_tok[i] = A.row_token[i];
+  __syncthreads();
+  return tok ? s_tok : A.row_token;
+}
+
 // Persistent: warp w of the grid takes items w, w + W, w + 2W, ...; an item
 // is (expert, 16 features); consecutive items share the expert so the warps
 // of a block re-read the same activation rows from L1.
 template <bool INT4>
 __global__ void __launch_bounds__(kThreads, 2) k_dec_gateup(const DecArgs A) {
+  const int32_t* off = A.offsets;
+  const int32_t* tok = A.row_token;
+  if constexpr (!INT4) {
+    __shared__ int s_off[kMaxE + 1], s_tok[kTokStage];
+    tok = stage_maps(A, s_off, s_tok);
+    off = s_off;
+  }
   const int W = gridDim.x * kWarpsPerBlock;
   const int per_e = A.f / 16;
   const int items = A.E * per_e;
   for (int it = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); it < items; it += W) {
     const int e = it / per_e, n0 = (it % per_e) * 16;
-    const int r0 = A.offsets[e], r1 = A.offsets[e + 1];
+    const int r0 = off[e], r1 = off[e + 1];
     for (int row0 = r0; row0 < r1; row0 += kMaxRowsPerPass<INT4>) {
       const int nrows = min(kMaxRowsPerPass<INT4>, r1 - row0);
       switch ((nrows + 7) / 8) {
-        case 1: gateup_chunk<INT4, 1>(A, e, n0, row0, nrows); break;
-        case 2: gateup_chunk<INT4, 2>(A, e, n0, row0, nrows); break;
-        case 3: if constexpr (!INT4) gateup_chunk<INT4, 3>(A, e, n0, row0, nrows); break;
-        default: if constexpr (!INT4) gateup_chunk<INT4, 4>(A, e, n0, row0, nrows); break;
+        case 1: gateup_chunk<INT4, 1>(A, tok, e, n0, row0, nrows); break;
+        case 2: gateup_chunk<INT4, 2>(A, tok, e, n0, row0, nrows); break;
+        case 3: if constexpr (!INT4) gateup_chunk<INT4, 3>(A, tok, e, n0, row0, nrows); break;
+        default: if constexpr (!INT4) gateup_chunk<INT4, 4>(A, tok, e, n0, row0, nrows); break;
       }
     }
   }
@@ -396,6 +423,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_dec_gateup(const DecArgs A) {
 // warps read the same part of H.
 template <bool INT4>
 __global__ void __launch_bounds__(kThreads, 2) k_dec_down(const DecArgs A) {
+  const int32_t* off = A.offsets;
+  if constexpr (!INT4) {
+    __shared__ int s_off[kMaxE + 1];
+    stage_maps(A, s_off, nullptr);
+    off = s_off;
+  }
   const int W = gridDim.x * kWarpsPerBlock;
   const int per_e = A.d / 32;
   const int per_split = A.E * per_e;
@@ -403,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_dec_down(const DecArgs A) {
   for (int it = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); it < items; it += W) {
     const int split = it / per_split, rem = it % per_split;
     const int e = rem / per_e, o0 = (rem % per_e) * 32;
-    const int r0 = A.offsets[e], r1 = A.offsets[e + 1];
+    const int r0 = off[e], r1 = off[e + 1];
     for (int row0 = r0; row0 < r1; row0 += kMaxRowsPerPass<INT4>) {
       const int nrows = min(kMaxRowsPerPass<INT4>, r1 - row0);
       switch ((nrows + 7) / 8) {
