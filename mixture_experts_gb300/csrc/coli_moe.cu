@@ -128,7 +128,7 @@ struct coli_moe {
   void* perm_scratch = nullptr;
   void* x_stage = nullptr;
   void* y_stage = nullptr;
-  float* xsum = nullptr;  // int4: 136 * group sums of x_perm, then of H
+  float* xsum = nullptr;  // int4: 136 * group sums of the gate/up activations, then of H
   // timing
   bool timing = false;
   TimingSet ring[kTimingRing];
@@ -209,8 +209,10 @@ void harvest(coli_moe* h, TimingSet& ts) {
   ts.pending = false;
 }
 
-// Expert FFN over grouped rows (x_perm, offsets) -> y (f32). When the decode
-// path splits the down projection, partial slices go to h->y_part and
+// Expert FFN over grouped rows (x_perm, offsets) -> y (f32). With row_token
+// set (decode path, bf16/int4 experts) the gate/up kernel reads row r's
+// activations from x_tok[row_token[r]] and x_perm is not used. When the
+// decode path splits the down projection, partial slices go to h->y_part and
 // *splits_out > 1 (the caller sums them: the combine directly, the FFN stage
 // through a reduction).
 int run_ffn(coli_moe* h, const void* x_perm, const int32_t* offsets, int n_rows, float* y_perm,
