@@ -220,10 +220,11 @@ int coli_combine(const float* y_perm, const int32_t* assign_row, const float* to
  * makes no allocation of any kind. Batches whose table would not fit
  * (coli_permute_scratch_bytes(T, k, E) > COLI_PERMUTE_STATIC_SCRATCH_BYTES,
  * i.e. T*k > 131072 at E = 256 or T*k > 524288 at E = 64) are rejected with
- * COLI_EINVAL. The first call on a device looks up the area's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture. All
- * calls share the one area, so calls whose kernels overlap on a GPU (other
- * streams, other threads) race and must be serialised by the caller. */
+ * COLI_EINVAL. The first call on a device looks up the area's device
+ * address (cudaGetSymbolAddress) with that device current and keeps it for
+ * later calls. All calls share the one area, so calls whose kernels overlap
+ * on a GPU (other streams, other threads) race and must be serialised by the
+ * caller. */
 #define COLI_PERMUTE_STATIC_SCRATCH_BYTES 65536
 int coli_permute_noalloc(const int32_t* topk_idx, const void* x, int32_t T, int32_t d,
                          int32_t E, int32_t k, int32_t act, int32_t* counts, int32_t* offsets,
