@@ -185,8 +185,9 @@ int coli_route_topk(const void* x, const void* w_router, const float* b_router, 
 /* Dispatch (discosf.com section 4.2 counting sort; overview section 3.3
  * token-to-expert map and expert offsets): counts [E], offsets [E+1]
  * (exclusive prefix), row_token [T*k], assign_row [T*k] and the gathered
- * rows x_perm [T*k][d] = x[row_token[r]]. Rows of one expert keep token
- * order, so the result is unique and bit-exact. Ids outside [0, E) are
+ * rows x_perm [T*k][d] = x[row_token[r]] (x_perm may be NULL: then only the
+ * counts, offsets and maps are produced and x is not read). Rows of one
+ * expert keep token order, so the result is unique and bit-exact. Ids outside [0, E) are
  * skipped and latch COLI_EDEVICE. Needs coli_permute_scratch_bytes(T, k, E)
  * bytes of device scratch (256-byte aligned). */
 size_t coli_permute_scratch_bytes(int32_t T, int32_t k, int32_t E);

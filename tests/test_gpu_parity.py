@@ -175,6 +175,28 @@ def test_stage_permute(T, E, k, act):
     assert moe.coli_device_status() == 0
 
 
+@pytest.mark.parametrize("T,E,k", [(37, 8, 2), (5000, 64, 4)])
+def test_stage_permute_without_row_copy(T, E, k):
+    # x_perm NULL: the maps alone, x never read (the forward's decode path)
+    idx = inputs.random_assignments(T, E, k, seed=T + 1).cuda()
+    n = T * k
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    row_token = torch.empty(n, dtype=torch.int32, device="cuda")
+    assign_row = torch.empty(n, dtype=torch.int32, device="cuda")
+    nb = moe.coli_permute_scratch_bytes(T, k, E)
+    scratch = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
+    rc = moe.coli_permute(idx, None, T, 128, E, k, moe.BF16, counts, offsets, row_token,
+                          assign_row, None, scratch, nb)
+    assert rc == 0, moe.last_error()
+    c, o, rt, ar = oracle.dispatch(idx.cpu().numpy(), E)
+    assert np.array_equal(counts.cpu().numpy(), c)
+    assert np.array_equal(offsets.cpu().numpy(), o)
+    assert np.array_equal(row_token.cpu().numpy(), rt)
+    assert np.array_equal(assign_row.cpu().numpy(), ar)
+    assert moe.coli_device_status() == 0
+
+
 @pytest.mark.parametrize("name", ["decode_bf16", "int4", "tiny_fp32"])
 def test_stage_expert_ffn(name):
     s = SMALL[name]
