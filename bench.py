@@ -39,6 +39,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--config", default="mixtral_decode")
     p.add_argument("--impl", default="coli", choices=["coli", "reference"])
+    p.add_argument("--ref-seconds", type=float, default=60.0,
+                   help="--impl reference: oracle time budget for the whole run, whatever "
+                        "--steps and --warmup are")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="budget of the oracle CPU-baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -131,32 +134,62 @@ def oracle_sample(s, layer, budget_s: float):
 
 
 def run_reference(args):
+    """The reference arm: the oracle (the plain CPU statement of the layer) as
+    it stands, one thread pinned to one core. One token's cost is measured
+    once; the tokens that fit in --ref-seconds are spread over the timed steps
+    (at most the workload's T per step, so a step may hold none when there are
+    more steps than tokens), and the warm-up steps only page the oracle in.
+    The run therefore ends in about --ref-seconds whatever --steps is; value =
+    tokens timed / time spent on them."""
+    import numpy as np
+    import oracle
     rank, world, _ = dist_env()
     if rank != 0:
         return
     from mixture_experts_gb300 import inputs
     s = inputs.CONFIGS[args.config]
     layer = inputs.make_layer(s, seed=0)
-    per_step = []
-    budget = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
-    n_total, t_total = 0, 0.0
-    for i in range(args.warmup + args.steps):
-        tps, n, dt = oracle_sample(s, layer, budget)
-        if i >= args.warmup:
-            per_step.append(dt)
+    oracle.build()
+    saved = None
+    if hasattr(os, "sched_setaffinity"):
+        saved = os.sched_getaffinity(0)
+        os.sched_setaffinity(0, {min(saved)})
+
+    def timed(n):
+        if n <= 0:
+            return 0.0
+        tokens = np.arange(n, dtype=np.int32) % s.T
+        t0 = time.perf_counter()
+        oracle.moe_forward(layer, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f, tokens=tokens)
+        return time.perf_counter() - t0
+
+    try:
+        t_one = max(timed(1), 1e-6)  # also the warm-up: pages the oracle and the layer in
+        for _ in range(max(0, args.warmup - 1)):
+            timed(0)
+        steps = max(1, args.steps)
+        budget_tokens = max(1, min(int(args.ref_seconds / t_one), steps * s.T))
+        per_step, n_total = [], 0
+        for i in range(steps):
+            n = (i + 1) * budget_tokens // steps - i * budget_tokens // steps
+            per_step.append(timed(n))
             n_total += n
-            t_total += dt
+    finally:
+        if saved is not None:
+            os.sched_setaffinity(0, saved)
+    t_total = sum(per_step)
     value = n_total / t_total
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * t_total / max(1, len(per_step)), "higher_is_better": True,
+        "ms_per_step": 1e3 * t_total / len(per_step), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
         "config": {"workload": workload_desc(s)},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{n_total // max(1, args.steps)} of the {s.T} tokens per "
-                                   f"step, whole layer per token, single thread",
+                         "sample": f"{n_total} tokens over {len(per_step)} timed steps (of "
+                                   f"the {s.T} tokens of a step), whole layer per token, "
+                                   f"one thread on one core",
                          "host": host_desc()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

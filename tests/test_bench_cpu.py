@@ -5,6 +5,7 @@ import os
 import socket
 import subprocess
 import sys
+import time
 
 import pytest
 import torch.multiprocessing as mp
@@ -66,6 +67,22 @@ def test_reference_arm_json_line():
         assert key in d
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_is_bounded_for_many_steps():
+    # the driver may pass any --steps/--warmup: the oracle's time stays within
+    # the --ref-seconds budget, and the line says how many tokens were timed
+    t0 = time.time()
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "tiny_fp32", "--steps", "2000", "--warmup", "20",
+                        "--ref-seconds", "1"], capture_output=True, text=True, timeout=300,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    assert time.time() - t0 < 120
+    d = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    assert d["steps"] == 2000 and d["value"] > 0
+    assert "over 2000 timed steps" in d["cpu_baseline"]["sample"]
+    assert d["ms_per_step"] * 2000 / 1e3 < 5.0  # oracle time summed over the timed steps
 
 
 def test_reference_arm_other_ranks_exit_quietly():
