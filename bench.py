@@ -328,11 +328,27 @@ def run_coli(args):
         layer(x, y)
     barrier()
 
+    def busy(seconds: float) -> int:
+        """Untimed forwards of the same workload for about `seconds`."""
+        n, t_end = 0, time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            for _ in range(8):
+                layer(x, y)
+            torch.cuda.synchronize()
+            n += 8
+        return n
+
+    # clocks are sampled under load only: the sampler starts while untimed
+    # forwards run, and a timed region shorter than the sampling needs is
+    # followed by more of them (stated in the line's clocks.window)
+    clocks = ClockSampler(local)
+    clocks.start()
+    pre = busy(0.5)
+    barrier()
+
     # ---- timed region: K forwards with stage timing on the launching stream
     moe.coli_moe_set_timing(layer.h, True)
     moe.coli_moe_stage_times(layer.h)  # reset sums
-    clocks = ClockSampler(local)
-    clocks.start()
     barrier()
     if flush:
         per = []
@@ -356,9 +372,13 @@ def run_coli(args):
         barrier()
         elapsed_ms = a.elapsed_time(b)
     barrier()
-    clk = clocks.stop()
     stage_ms, n_fwd, n_launch = moe.coli_moe_stage_times(layer.h)
     moe.coli_moe_set_timing(layer.h, False)
+    post = busy(0.5 - elapsed_ms / 1e3) if elapsed_ms < 500.0 else 0
+    clk = clocks.stop()
+    clk["window"] = (f"{pre} untimed forwards while the sampler started, the timed region"
+                     + (f", then {post} more untimed forwards (the timed region lasted "
+                        f"{elapsed_ms:.1f} ms)" if post else ""))
     tokens, seconds = aggregate(s.T * args.steps, elapsed_ms / 1e3, world)
     value = tokens / seconds
 
