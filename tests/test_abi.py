@@ -87,3 +87,39 @@ def test_handle_calls_reject_null(lib):
     assert moe.coli_moe_path_for(None, 4) == moe.COLI_EINVAL
     assert lib.coli_moe_set_timing(None, 1) == moe.COLI_EINVAL
     moe.coli_moe_destroy(None)  # no-op
+
+
+def _declarations():
+    """name -> list of parameter types, parsed from include/coli_moe.h."""
+    import re
+    text = open(moe.HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"#.*", "", text)
+    out = {}
+    for m in re.finditer(r"([\w\s\*]+?)\b(coli_\w+)\s*\(([^;{]*?)\)\s*;", text):
+        params = " ".join(m.group(3).split())
+        out[m.group(2)] = ([] if params in ("", "void") else
+                           [p.strip() for p in params.split(",")])
+    return out
+
+
+def _kind(param: str) -> str:
+    """The ctypes class a C parameter needs: P pointer, Z size_t, I 32-bit int."""
+    if "*" in param:
+        return "P"
+    words = param.split()
+    if words[0] == "size_t":
+        return "Z"
+    if words[0] in ("int", "int32_t"):
+        return "I"
+    raise AssertionError(f"unexpected parameter type: {param}")
+
+
+def test_binding_signatures_match_header():
+    # every ctypes signature of the binding has the header's parameter count
+    # and kinds, so no call passes arguments of the wrong size
+    decl = _declarations()
+    assert set(moe._SIGS) == set(decl) == set(moe.header_functions())
+    for name, (_, args) in moe._SIGS.items():
+        want = [_kind(p) for p in decl[name]]
+        assert args == want, (name, args, want)
