@@ -158,7 +158,10 @@ int coli_moe_path_for(const coli_moe* h, int32_t T);
  * coli_moe_stage_times synchronises on the last recorded event, adds the
  * elapsed milliseconds of every timed forward since the last call into
  * ms[0..n), the number of timed forwards into *n_forwards and the number of
- * kernel launches into *n_launches, then resets the sums. */
+ * kernel launches into *n_launches, then resets the sums. The first
+ * coli_moe_set_timing(h, 1) creates every event the timed forwards record
+ * (so a timed forward still allocates nothing); call it outside any section
+ * that may not allocate. */
 int coli_moe_set_timing(coli_moe* h, int enable);
 int coli_moe_stage_times(coli_moe* h, float* ms, int n, int32_t* n_forwards, int64_t* n_launches);
 
@@ -173,9 +176,10 @@ void coli_moe_destroy(coli_moe* h);
  * x [T][d], w_router [E][d] (act dtype), b_router [E] f32 or NULL ->
  * topk_idx [T][k] i32 (descending logit, lower index first on ties),
  * topk_w [T][k] f32 (renormalised gates), gap [T] f32 or NULL.
- * Logits are fp32 dot products (+ bias in fp32). Needs
- * coli_route_scratch_bytes(T, d, E) bytes of device scratch (0 when E <= 32;
- * scratch may then be NULL). */
+ * Logits are fp32 dot products (+ bias in fp32). A NaN logit ranks below
+ * every other (as -inf) and latches COLI_EDEVICE, so each token still gets k
+ * distinct ids in [0, E). Needs coli_route_scratch_bytes(T, d, E) bytes of
+ * device scratch (0 when E <= 32; scratch may then be NULL). */
 size_t coli_route_scratch_bytes(int32_t T, int32_t d, int32_t E);
 int coli_route_topk(const void* x, const void* w_router, const float* b_router, int32_t T,
                     int32_t d, int32_t E, int32_t k, int32_t act, int32_t* topk_idx,
@@ -188,7 +192,8 @@ int coli_route_topk(const void* x, const void* w_router, const float* b_router, 
  * rows x_perm [T*k][d] = x[row_token[r]] (x_perm may be NULL: then only the
  * counts, offsets and maps are produced and x is not read). Rows of one
  * expert keep token order, so the result is unique and bit-exact. Ids outside [0, E) are
- * skipped and latch COLI_EDEVICE. Needs coli_permute_scratch_bytes(T, k, E)
+ * skipped (their assign_row entry is set to -1, and counts and offsets leave
+ * them out) and latch COLI_EDEVICE. Needs coli_permute_scratch_bytes(T, k, E)
  * bytes of device scratch (256-byte aligned). */
 size_t coli_permute_scratch_bytes(int32_t T, int32_t k, int32_t E);
 int coli_permute(const int32_t* topk_idx, const void* x, int32_t T, int32_t d, int32_t E,
@@ -207,7 +212,9 @@ int coli_expert_ffn(const coli_moe* h, const void* x_perm, const int32_t* offset
 /* Combine (overview section 2.1 weighted merge; mhpn.cn section 2.3 copy back
  * in token order): y[t] = sum_{j ascending} topk_w[t][j] *
  * y_perm[assign_row[t*k+j]], summed in fp32, written in `out` dtype
- * (bf16 by round-to-nearest-even). */
+ * (bf16 by round-to-nearest-even). y_perm has T*k rows; an assign_row entry
+ * outside [0, T*k) (such as the -1 of an assignment coli_permute skipped)
+ * contributes nothing, is never dereferenced, and latches COLI_EDEVICE. */
 int coli_combine(const float* y_perm, const int32_t* assign_row, const float* topk_w,
                  int32_t T, int32_t k, int32_t d, int32_t out, void* y, void* stream);
 
@@ -218,14 +225,22 @@ int coli_combine(const float* y_perm, const int32_t* assign_row, const float* to
  * Same inputs, outputs and results as coli_permute, but the scratch table
  * lives in a fixed COLI_PERMUTE_STATIC_SCRATCH_BYTES area inside the library
  * that each GPU loading the library holds until the process exits; the call
- * makes no allocation of any kind. Batches whose table would not fit
- * (coli_permute_scratch_bytes(T, k, E) > COLI_PERMUTE_STATIC_SCRATCH_BYTES,
- * i.e. T*k > 131072 at E = 256 or T*k > 524288 at E = 64) are rejected with
- * COLI_EINVAL. The first call on a device looks up the area's device
- * address (cudaGetSymbolAddress) with that device current and keeps it for
- * later calls. All calls share the one area, so calls whose kernels overlap
- * on a GPU (other streams, other threads) race and must be serialised by the
- * caller. */
+ * itself makes no cudaMalloc, cudaFree or other allocating call. Batches whose
+ * table would not fit (coli_permute_scratch_bytes(T, k, E) >
+ * COLI_PERMUTE_STATIC_SCRATCH_BYTES, i.e. T*k > 131072 at E = 256 or
+ * T*k > 524288 at E = 64) are rejected with COLI_EINVAL.
+ * Set-up: the first call on a device looks up the area's device address
+ * (cudaGetSymbolAddress) with that device current and keeps it for later
+ * calls. Under CUDA's lazy module loading that lookup may also load the
+ * library's device code onto the GPU, which allocates the device image
+ * (including this area). A caller that may not allocate after start-up
+ * should therefore make one call per device at start-up, before any stream
+ * capture: a call with T = 0 (and valid pointers) is enough. The kept address
+ * is invalid after cudaDeviceReset; do not use this entry point afterwards in
+ * the same process.
+ * All calls share the one area and it keeps the last call's table, so calls
+ * whose kernels overlap on a GPU (other streams, other threads) race and must
+ * be serialised by the caller. */
 #define COLI_PERMUTE_STATIC_SCRATCH_BYTES 65536
 int coli_permute_noalloc(const int32_t* topk_idx, const void* x, int32_t T, int32_t d,
                          int32_t E, int32_t k, int32_t act, int32_t* counts, int32_t* offsets,

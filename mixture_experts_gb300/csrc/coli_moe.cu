@@ -80,7 +80,7 @@ constexpr int kSplitRows = 8192;  // rows x slices the split-reduction buffer ho
 constexpr int kMaxSplits = 32;
 
 struct TimingSet {
-  cudaEvent_t ev[kStages + 1];
+  cudaEvent_t ev[kStages + 1] = {};
   bool pending;
   int launches;
 };
@@ -148,9 +148,9 @@ struct coli_moe {
   ~coli_moe() {
     if (tc) tc_plan_destroy(tc);
     for (void* p : allocs) cudaFree(p);
-    if (ring_init)
-      for (auto& s : ring)
-        for (auto& e : s.ev) cudaEventDestroy(e);
+    for (auto& s : ring)
+      for (auto& e : s.ev)
+        if (e != nullptr) cudaEventDestroy(e);
   }
 };
 
@@ -234,7 +234,10 @@ int run_ffn(coli_moe* h, const void* x_perm, const int32_t* offsets, int n_rows,
   }
   const int path = pick_path(h, T);
   if (path == COLI_PATH_PREFILL) {
-    CUDA_TRY(launch_tc_gateup(h->tc, x_perm, offsets, h->H, n_rows, st, status));
+    // the handle's x_perm has a tensor map made at create; a caller's buffer
+    // (the exposed FFN stage) gets one encoded here
+    CUDA_TRY(launch_tc_gateup(h->tc, x_perm, x_perm == h->x_perm, offsets, h->H, n_rows, st,
+                              status));
     timing_mark(h, ts, 3, st);
     CUDA_TRY(launch_tc_down(h->tc, h->H, offsets, y_perm, n_rows, st, status));
     timing_mark(h, ts, 4, st);
@@ -397,7 +400,8 @@ int coli_moe_create(const coli_moe_config* cfg, const coli_moe_weights* wts, voi
   h->w.s_gu = static_cast<const __nv_bfloat16*>(sgu);
   h->w.s_dn = static_cast<const __nv_bfloat16*>(sdn);
   if (cfg->weight_dtype == COLI_BF16 && tc_supported(d, f)) {
-    if ((e = tc_plan_create(&h->tc, wgu, wdn, E, d, f, static_cast<int>(Na))) != cudaSuccess)
+    if ((e = tc_plan_create(&h->tc, wgu, wdn, E, d, f, static_cast<int>(Na), h->x_perm,
+                            h->H)) != cudaSuccess)
       return bail(COLI_ECUDA, "tensor-core plan", e);
   }
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return bail(COLI_ECUDA, "create sync", e);
@@ -419,14 +423,7 @@ int coli_moe_forward(coli_moe* h, const void* x, int32_t T, void* y, void* strea
   const int E = c.n_experts, d = c.d_model, k = c.top_k, n_rows = T * k;
   int* status = device_status_ptr();
   TimingSet* ts = nullptr;
-  if (h->timing) {
-    if (!h->ring_init) {
-      for (auto& s : h->ring) {
-        for (auto& ev : s.ev) CUDA_TRY(cudaEventCreate(&ev));
-        s.pending = false;
-      }
-      h->ring_init = true;
-    }
+  if (h->timing && h->ring_init) {  // events were made by coli_moe_set_timing
     ts = &h->ring[h->ring_next];
     h->ring_next = (h->ring_next + 1) % kTimingRing;
     harvest(h, *ts);
@@ -435,7 +432,7 @@ int coli_moe_forward(coli_moe* h, const void* x, int32_t T, void* y, void* strea
   int launches = 0;
   timing_mark(h, ts, 0, st);
   CUDA_TRY(launch_route(x, h->w_router, h->b_router, T, d, E, k, c.act_dtype, h->topk_idx,
-                        h->topk_w, h->gap, h->route_scratch, st, &launches));
+                        h->topk_w, h->gap, h->route_scratch, st, status, &launches));
   timing_mark(h, ts, 1, st);
   // the decode kernels read token rows of x themselves: no x_perm copy
   const bool gather = c.weight_dtype != COLI_F32 && pick_path(h, T) == COLI_PATH_DECODE;
@@ -449,7 +446,7 @@ int coli_moe_forward(coli_moe* h, const void* x, int32_t T, void* y, void* strea
   if (rc) return rc;
   const float* part = splits > 1 ? h->y_part : h->y_perm;
   CUDA_TRY(launch_combine(part, splits, static_cast<size_t>(n_rows) * d, h->assign_row,
-                          h->topk_w, T, k, d, c.act_dtype, y, st));
+                          h->topk_w, T, k, d, c.act_dtype, y, st, status));
   launches += 1;
   timing_mark(h, ts, 5, st);
   if (ts) {
@@ -526,7 +523,24 @@ int coli_moe_path_for(const coli_moe* h, int32_t T) {
 }
 
 int coli_moe_set_timing(coli_moe* h, int enable) {
-  if (h == nullptr) return fail(nullptr, 0, COLI_EINVAL, "handle is NULL");
+  char* err = nullptr;
+  size_t err_len = 0;
+  if (h == nullptr) return fail(err, err_len, COLI_EINVAL, "handle is NULL");
+  if (enable && !h->ring_init) {
+    // every event the timed forwards will record is made here, so a forward
+    // never creates one
+    for (auto& ts : h->ring) {
+      for (auto& ev : ts.ev) {
+        const cudaError_t e = cudaEventCreate(&ev);
+        if (e != cudaSuccess) {
+          ev = nullptr;
+          return fail(err, err_len, COLI_ECUDA, "cudaEventCreate: %s", cudaGetErrorString(e));
+        }
+      }
+      ts.pending = false;
+    }
+    h->ring_init = true;
+  }
   h->timing = enable != 0;
   return COLI_OK;
 }
@@ -571,7 +585,7 @@ int coli_route_topk(const void* x, const void* w_router, const float* b_router, 
   if (need > 0 && (scratch == nullptr || scratch_bytes < need))
     return fail(err, err_len, COLI_EINVAL, "router needs %zu bytes of scratch", need);
   CUDA_TRY(launch_route(x, w_router, b_router, T, d, E, k, act, topk_idx, topk_w, gap, scratch,
-                        static_cast<cudaStream_t>(stream), nullptr));
+                        static_cast<cudaStream_t>(stream), device_status_ptr(), nullptr));
   return COLI_OK;
 }
 
@@ -635,7 +649,7 @@ int coli_combine(const float* y_perm, const int32_t* assign_row, const float* to
                  int32_t k, int32_t d, int32_t out, void* y, void* stream) {
   char* err = nullptr;
   size_t err_len = 0;
-  if (T < 0 || k < 1 || k > 256 || d <= 0 || d % 4)
+  if (T < 0 || k < 1 || k > 256 || d <= 0 || d % 4 || static_cast<long>(T) * k > (1L << 30))
     return fail(err, err_len, COLI_EINVAL, "bad sizes T=%d k=%d d=%d", T, k, d);
   if (out != COLI_F32 && out != COLI_BF16) return fail(err, err_len, COLI_EINVAL, "bad out dtype");
   if (T == 0) return ok(err, err_len);
@@ -644,7 +658,7 @@ int coli_combine(const float* y_perm, const int32_t* assign_row, const float* to
   if (!aligned16(y_perm) || (reinterpret_cast<uintptr_t>(y) & (out == COLI_F32 ? 15u : 7u)))
     return fail(err, err_len, COLI_EINVAL, "y_perm must be 16-byte and y 16/8-byte aligned");
   CUDA_TRY(launch_combine(y_perm, 1, 0, assign_row, topk_w, T, k, d, out, y,
-                          static_cast<cudaStream_t>(stream)));
+                          static_cast<cudaStream_t>(stream), device_status_ptr()));
   return COLI_OK;
 }
 

@@ -25,9 +25,11 @@ int* device_status_ptr();  // nullptr if the symbol address cannot be taken
 
 // ---- router (A1) ------------------------------------------------------------
 size_t route_scratch_bytes(int T, int d, int E);
+// A NaN logit ranks below every other (as -inf) and latches COLI_EDEVICE, so
+// every token still gets k distinct ids in [0, E).
 cudaError_t launch_route(const void* x, const void* w_r, const float* b_r, int T, int d, int E,
                          int k, int act, int32_t* topk_idx, float* topk_w, float* gap,
-                         void* scratch, cudaStream_t st, int* n_launches);
+                         void* scratch, cudaStream_t st, int* status, int* n_launches);
 
 // ---- dispatch (A2) ------------------------------------------------------------
 size_t permute_scratch_bytes(int T, int k, int E);
@@ -76,20 +78,27 @@ cudaError_t launch_f32_ffn(const float* w_gu, const float* w_dn, const float* x_
 // Prefill path: TMA + tcgen05/TMEM grouped GEMM (bf16 weights).
 struct TcPlan;  // defined in k_ffn_tc.cu
 bool tc_supported(int d, int f);
+// x_perm [max_rows][d] and H [max_rows][f] are the handle's buffers: their
+// tensor maps are encoded once here (rows past a forward's last group are
+// computed from stale data but never stored).
 cudaError_t tc_plan_create(TcPlan** plan, const void* w_gu, const void* w_dn, int E, int d, int f,
-                           int max_rows);
+                           int max_rows, const void* x_perm, const void* H);
 void tc_plan_destroy(TcPlan* plan);
 // H[rows][f] = silu(x_perm Wg^T) * (x_perm Wu^T) per expert group (bf16).
-cudaError_t launch_tc_gateup(TcPlan* plan, const void* x_perm, const int32_t* offsets, void* H,
-                             int n_rows, cudaStream_t st, int* status);
-// y_perm[rows][d] = H Wd^T per expert group (f32).
+// own_x_perm: x_perm is the plan's buffer (its map is reused), else a map is
+// encoded for this call.
+cudaError_t launch_tc_gateup(TcPlan* plan, const void* x_perm, bool own_x_perm,
+                             const int32_t* offsets, void* H, int n_rows, cudaStream_t st,
+                             int* status);
+// y_perm[rows][d] = H Wd^T per expert group (f32); H is the plan's buffer.
 cudaError_t launch_tc_down(TcPlan* plan, const void* H, const int32_t* offsets, float* y_perm,
                            int n_rows, cudaStream_t st, int* status);
 
 // ---- combine (A4) and helpers ----------------------------------------------------
+// Rows outside [0, T*k) are skipped and latch COLI_EDEVICE in *status.
 cudaError_t launch_combine(const float* y_part, int splits, size_t part_stride,
                            const int32_t* assign_row, const float* topk_w, int T, int k, int d,
-                           int out_dt, void* y, cudaStream_t st);
+                           int out_dt, void* y, cudaStream_t st, int* status);
 cudaError_t launch_reduce_splits(const float* y_part, int splits, size_t part_stride,
                                  int n_rows, int d, float* y_perm, cudaStream_t st);
 cudaError_t launch_repack(const void* src_gate, const void* src_up, const void* src_down,

@@ -16,8 +16,10 @@
 // contribute none (their weights are never read: wzjinhao.cn page,
 // section 2.3) — and walks it with a static stride of gridDim.x, consecutive
 // tiles sharing the weight tile so the L2 serves the other row tiles. Row
-// tiles that run past an expert's rows are computed but not stored; rows past
-// the last group are zero-filled by TMA.
+// tiles that run past an expert's rows are computed but not stored (an output
+// row depends on its own input row only, so whatever those rows hold — the
+// next expert's rows, or stale workspace past the last group — never reaches
+// a stored value); rows past the end of the buffer are zero-filled by TMA.
 //
 // Gate/up epilogue: the weights are interleaved in 64-row blocks (gate rows,
 // then the matching up rows), so accumulator columns c and c + 64 of each
@@ -311,15 +313,14 @@ cudaError_t encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_byte
 }
 
 struct TcPlan {
-  CUtensorMap map_wgu, map_wdn;
+  CUtensorMap map_wgu, map_wdn, map_xperm, map_h;
   int E, d, f, grid;
 };
 
 bool tc_supported(int d, int f) { return d % 64 == 0 && f % 64 == 0 && encode_fn() != nullptr; }
 
 cudaError_t tc_plan_create(TcPlan** plan, const void* w_gu, const void* w_dn, int E, int d, int f,
-                           int max_rows) {
-  (void)max_rows;
+                           int max_rows, const void* x_perm, const void* H) {
   *plan = nullptr;
   TcPlan* p = new TcPlan();
   p->E = E;
@@ -336,6 +337,9 @@ cudaError_t tc_plan_create(TcPlan** plan, const void* w_gu, const void* w_dn, in
   if ((e = make_map(&p->map_wgu, w_gu, static_cast<uint64_t>(E) * 2 * f, d, BN)) !=
           cudaSuccess ||
       (e = make_map(&p->map_wdn, w_dn, static_cast<uint64_t>(E) * d, f, BN)) != cudaSuccess ||
+      (e = make_map(&p->map_xperm, x_perm, static_cast<uint64_t>(max_rows), d, BM)) !=
+          cudaSuccess ||
+      (e = make_map(&p->map_h, H, static_cast<uint64_t>(max_rows), f, BM)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(k_tc_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(kSmemBytes))) != cudaSuccess ||
       (e = cudaFuncSetAttribute(k_tc_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -349,12 +353,17 @@ cudaError_t tc_plan_create(TcPlan** plan, const void* w_gu, const void* w_dn, in
 
 void tc_plan_destroy(TcPlan* plan) { delete plan; }
 
-cudaError_t launch_tc_gateup(TcPlan* p, const void* x_perm, const int32_t* offsets, void* H,
-                             int n_rows, cudaStream_t st, int* status) {
+cudaError_t launch_tc_gateup(TcPlan* p, const void* x_perm, bool own_x_perm,
+                             const int32_t* offsets, void* H, int n_rows, cudaStream_t st,
+                             int* status) {
   if (n_rows == 0) return cudaSuccess;
   CUtensorMap map_a;
-  cudaError_t e = make_map(&map_a, x_perm, static_cast<uint64_t>(n_rows), p->d, BM);
-  if (e != cudaSuccess) return e;
+  if (own_x_perm) {
+    map_a = p->map_xperm;
+  } else {
+    const cudaError_t e = make_map(&map_a, x_perm, static_cast<uint64_t>(n_rows), p->d, BM);
+    if (e != cudaSuccess) return e;
+  }
   k_tc_gemm<0><<<p->grid, kThreads, kSmemBytes, st>>>(map_a, p->map_wgu, offsets, p->E, p->d,
                                                        2 * p->f, H, status);
   return cudaGetLastError();
@@ -362,11 +371,9 @@ cudaError_t launch_tc_gateup(TcPlan* p, const void* x_perm, const int32_t* offse
 
 cudaError_t launch_tc_down(TcPlan* p, const void* H, const int32_t* offsets, float* y_perm,
                            int n_rows, cudaStream_t st, int* status) {
+  (void)H;  // always the plan's H buffer, mapped at create
   if (n_rows == 0) return cudaSuccess;
-  CUtensorMap map_a;
-  cudaError_t e = make_map(&map_a, H, static_cast<uint64_t>(n_rows), p->f, BM);
-  if (e != cudaSuccess) return e;
-  k_tc_gemm<1><<<p->grid, kThreads, kSmemBytes, st>>>(map_a, p->map_wdn, offsets, p->E, p->f,
+  k_tc_gemm<1><<<p->grid, kThreads, kSmemBytes, st>>>(p->map_h, p->map_wdn, offsets, p->E, p->f,
                                                        p->d, y_perm, status);
   return cudaGetLastError();
 }

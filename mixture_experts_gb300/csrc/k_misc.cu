@@ -12,12 +12,14 @@ namespace {
 // y[t] = sum_{j ascending} g[t][j] * (sum_{s ascending} part[s][row]), row =
 // assign_row[t*k+j]: the overview page's weighted merge (trdm.cn section 2.1)
 // and the copy back in token order of the mhpn.cn page (section 2.3). A
-// gather, so no atomics and a fixed summation order.
+// gather, so no atomics and a fixed summation order. A row outside
+// [0, n_rows) (an assignment the dispatch skipped, or bad caller data) adds
+// nothing and latches COLI_EDEVICE; it is never read.
 template <bool BF16_OUT>
 __global__ void __launch_bounds__(256)
     k_combine(const float* __restrict__ part, int splits, size_t part_stride,
               const int32_t* __restrict__ assign_row, const float* __restrict__ topk_w, int T,
-              int k, int d, void* __restrict__ y) {
+              int k, int d, int n_rows, void* __restrict__ y, int* status) {
   // block (token t, 1024-wide column slab); one float4 column per thread
   const int t = blockIdx.x;
   const int d4 = d / 4;
@@ -28,7 +30,12 @@ __global__ void __launch_bounds__(256)
   for (int j = 0; j < k; ++j) {
     const size_t a = static_cast<size_t>(t) * k + j;
     const float g = topk_w[a];
-    const size_t base = static_cast<size_t>(assign_row[a]) * d4 + c;
+    const int row = assign_row[a];
+    if (row < 0 || row >= n_rows) {
+      if (c == 0) latch_error(status, kErrDevice);
+      continue;
+    }
+    const size_t base = static_cast<size_t>(row) * d4 + c;
     float4 v = reinterpret_cast<const float4*>(part)[base];
 #pragma unroll 4
     for (int s = 1; s < splits; ++s) {
@@ -238,17 +245,18 @@ __global__ void k_selftest_wait(int spin_limit, int* status) {
 
 cudaError_t launch_combine(const float* y_part, int splits, size_t part_stride,
                            const int32_t* assign_row, const float* topk_w, int T, int k, int d,
-                           int out_dt, void* y, cudaStream_t st) {
+                           int out_dt, void* y, cudaStream_t st, int* status) {
   if (T == 0) return cudaSuccess;
   const int d4 = d / 4;
   const int threads = d4 >= 256 ? 256 : ((d4 + 31) / 32) * 32;
   const dim3 grid(T, (d4 + threads - 1) / threads);
+  const int n_rows = T * k;  // assign_row maps the T*k assignments onto rows [0, T*k)
   if (out_dt == DT_BF16)
     k_combine<true><<<grid, threads, 0, st>>>(y_part, splits, part_stride, assign_row, topk_w,
-                                              T, k, d, y);
+                                              T, k, d, n_rows, y, status);
   else
     k_combine<false><<<grid, threads, 0, st>>>(y_part, splits, part_stride, assign_row, topk_w,
-                                               T, k, d, y);
+                                               T, k, d, n_rows, y, status);
   return cudaGetLastError();
 }
 

@@ -95,6 +95,8 @@ COLI_DEV void scatter_range(const int32_t* __restrict__ topk_idx, int a0, int a1
       const int row = base[e] + wcnt[w][e] + rank;
       row_token[row] = a / k;
       assign_row[a] = row;
+    } else if (a < a1) {
+      assign_row[a] = -1;  // skipped (bad id): a later combine adds nothing for it
     }
     __syncthreads();
     if (tid < E) base[tid] += tot[tid];

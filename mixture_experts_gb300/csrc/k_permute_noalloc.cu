@@ -54,9 +54,14 @@ int coli_permute_noalloc(const int32_t* topk_idx, const void* x, int32_t T, int3
                          int32_t k, int32_t act, int32_t* counts, int32_t* offsets,
                          int32_t* row_token, int32_t* assign_row, void* x_perm, void* stream) {
   if (T < 0 || d <= 0 || d % 64 || E < 1 || E > 256 || k < 1 || k > E ||
-      static_cast<long>(T) * k > (1L << 24))
-    return reject(COLI_EINVAL, "bad sizes: need T >= 0, d a positive multiple of 64, "
-                               "1 <= E <= 256, 1 <= k <= E");
+      static_cast<long>(T) * k > (1L << 24)) {
+    char msg[256];
+    snprintf(msg, sizeof msg,
+             "bad sizes T=%d d=%d E=%d k=%d: need T >= 0, d a positive multiple of 64, "
+             "1 <= E <= 256, 1 <= k <= E and T*k <= 16777216",
+             T, d, E, k);
+    return reject(COLI_EINVAL, msg);
+  }
   if (act != COLI_F32 && act != COLI_BF16) return reject(COLI_EINVAL, "bad act dtype");
   const size_t need = coli::permute_scratch_bytes(T, k, E);
   if (need > COLI_PERMUTE_STATIC_SCRATCH_BYTES) {

@@ -50,6 +50,17 @@ COLI_DEV bool beats(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
+// A NaN logit (e.g. from an overflowed input row) would compare false both
+// ways and break the ranking; it is ranked as -inf instead, and the token's
+// data error is latched.
+COLI_DEV float rankable(float v, int* status) {
+  if (v != v) {
+    latch_error(status, kErrDevice);
+    return -INFINITY;
+  }
+  return v;
+}
+
 // Value of the lane that holds `rank` (exactly one lane does).
 COLI_DEV float from_rank(int my_rank, float my_val, int rank) {
   const unsigned m = __ballot_sync(0xffffffffu, my_rank == rank);
@@ -60,7 +71,7 @@ template <typename TA, int EMAX>
 __global__ void __launch_bounds__(kWarps * 32)
     k_route_fused(const TA* __restrict__ x, const TA* __restrict__ w, const float* __restrict__ b,
                   int T, int d, int E, int k, int32_t* __restrict__ topk_idx,
-                  float* __restrict__ topk_w, float* __restrict__ gap) {
+                  float* __restrict__ topk_w, float* __restrict__ gap, int* status) {
   // one block per token: the 8 warps take interleaved 8-wide slices of the
   // reduction index, then warp 0 adds the 8 partial sums in warp order
   __shared__ float part[kWarps][EMAX];
@@ -105,7 +116,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     float v = 0.f;
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) v += part[i][lane];
-    le = (b != nullptr) ? v + b[lane] : v;
+    le = rankable((b != nullptr) ? v + b[lane] : v, status);
   }
   int rank = 0;
   for (int e = 0; e < E; ++e) {
@@ -252,7 +263,7 @@ template <int PER_LANE>
 __global__ void __launch_bounds__(kWarps * 32)
     k_route_select(const float* __restrict__ part, int slices, const float* __restrict__ b,
                    int T, int E, int k, int32_t* __restrict__ topk_idx,
-                   float* __restrict__ topk_w, float* __restrict__ gap) {
+                   float* __restrict__ topk_w, float* __restrict__ gap, int* status) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -265,6 +276,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       v = 0.f;
       for (int s = 0; s < slices; ++s) v += part[(static_cast<size_t>(s) * T + t) * E + e];
       if (b != nullptr) v += b[e];
+      v = rankable(v, status);
     }
     l[i] = v;
   }
@@ -330,7 +342,7 @@ size_t route_scratch_bytes(int T, int d, int E) {
 
 cudaError_t launch_route(const void* x, const void* w_r, const float* b_r, int T, int d, int E,
                          int k, int act, int32_t* topk_idx, float* topk_w, float* gap,
-                         void* scratch, cudaStream_t st, int* n_launches) {
+                         void* scratch, cudaStream_t st, int* status, int* n_launches) {
   if (T == 0) return cudaSuccess;
   const dim3 block(kWarps * 32);
   const dim3 grid((T + kWarps - 1) / kWarps);
@@ -338,7 +350,7 @@ cudaError_t launch_route(const void* x, const void* w_r, const float* b_r, int T
 #define COLI_ROUTE_FUSED(TA, EM)                                                             \
   k_route_fused<TA, EM><<<T, block, 0, st>>>(static_cast<const TA*>(x),                 \
                                                static_cast<const TA*>(w_r), b_r, T, d, E, k, \
-                                               topk_idx, topk_w, gap)
+                                               topk_idx, topk_w, gap, status)
     if (act == DT_F32) {
       if (E <= 8) COLI_ROUTE_FUSED(float, 8);
       else if (E <= 16) COLI_ROUTE_FUSED(float, 16);
@@ -365,11 +377,14 @@ cudaError_t launch_route(const void* x, const void* w_r, const float* b_r, int T
                                                part);
   }
   if (E <= 64)
-    k_route_select<2><<<grid, block, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap);
+    k_route_select<2><<<grid, block, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap,
+                                              status);
   else if (E <= 128)
-    k_route_select<4><<<grid, block, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap);
+    k_route_select<4><<<grid, block, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap,
+                                              status);
   else
-    k_route_select<8><<<grid, block, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap);
+    k_route_select<8><<<grid, block, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap,
+                                              status);
   if (n_launches) *n_launches += 2;
   return cudaGetLastError();
 }

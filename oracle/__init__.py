@@ -1,7 +1,10 @@
 """Oracle for one sparse MoE layer forward: TEST INFRASTRUCTURE ONLY.
 
-A plain, slow, single-threaded CPU statement of the layer (``moe_oracle.cpp``,
-fp64 accumulation), wrapped with ctypes. Only ``tests/``, the smoke check and
+A plain, slow CPU statement of the layer (``moe_oracle.cpp``, fp64
+accumulation), wrapped with ctypes. It runs on one thread; ``moe_forward``
+can also split its token list over several threads, each running the same
+per-token code, which gives bit-identical outputs (used to check full-size
+layers in reasonable time). Only ``tests/``, the smoke check and
 the benchmark's CPU-baseline leg may import this package. It shares no code
 with the CUDA library and never imports it.
 
@@ -37,7 +40,7 @@ def build(force: bool = False) -> str:
     if force or stale:
         tmp = _LIB + f".tmp{os.getpid()}"
         cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fPIC", "-shared",
-               "-o", tmp, _SRC]
+               "-pthread", "-o", tmp, _SRC]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
@@ -65,8 +68,10 @@ def _lib():
             h.oracle_combine.argtypes = [_f32p, _i32p, _f32p, i, i, i, i, vp, vp]
             h.oracle_moe_forward.argtypes = [vp, i, i, i, vp, vp, i, i, vp, vp, vp, vp, vp,
                                              vp, i, i, vp, i, vp, vp, vp, vp, vp]
+            h.oracle_moe_forward_mt.argtypes = h.oracle_moe_forward.argtypes + [i]
             for name in ("oracle_router_logits", "oracle_select_topk", "oracle_dispatch",
-                         "oracle_expert_ffn", "oracle_combine", "oracle_moe_forward"):
+                         "oracle_expert_ffn", "oracle_combine", "oracle_moe_forward",
+                         "oracle_moe_forward_mt"):
                 getattr(h, name).restype = i
             _handle = h
     return _handle
@@ -166,9 +171,11 @@ def combine(y_perm, assign_row, topk_w, T, k, d, out_dt):
     return y64, yo
 
 
-def moe_forward(layer, act_dt, w_dt, T, d, E, k, f, tokens=None):
+def moe_forward(layer, act_dt, w_dt, T, d, E, k, f, tokens=None, threads=1):
     """Whole layer for ``tokens`` (all when None). Returns a dict with y_f64
-    [n][d], y (act dtype: float32 or uint16 bf16 bits), topk_idx, topk_w, gap."""
+    [n][d], y (act dtype: float32 or uint16 bf16 bits), topk_idx, topk_w, gap.
+    ``threads`` > 1 splits the token list into that many contiguous ranges,
+    one thread each, with bit-identical results."""
     x, w_r, b_r = to_np(layer["x"]), to_np(layer["w_router"]), to_np(layer.get("b_router"))
     if b_r is not None:
         b_r = np.ascontiguousarray(b_r, dtype=np.float32)
@@ -181,8 +188,12 @@ def moe_forward(layer, act_dt, w_dt, T, d, E, k, f, tokens=None):
     idx = np.empty((n, k), np.int32)
     w = np.empty((n, k), np.float32)
     gap = np.empty(n, np.float32)
-    _check(_lib().oracle_moe_forward(_ptr(x), act_dt, T, d, _ptr(w_r), _ptr(b_r), E, k,
-                                     *[_ptr(a) for a in ws], w_dt, f, _ptr(tok),
-                                     0 if tok is None else len(tok), _ptr(y64), _ptr(yo),
-                                     _ptr(idx), _ptr(w), _ptr(gap)), "moe_forward")
+    args = (_ptr(x), act_dt, T, d, _ptr(w_r), _ptr(b_r), E, k, *[_ptr(a) for a in ws], w_dt, f,
+            _ptr(tok), 0 if tok is None else len(tok), _ptr(y64), _ptr(yo), _ptr(idx), _ptr(w),
+            _ptr(gap))
+    if threads > 1:
+        rc = _lib().oracle_moe_forward_mt(*args, int(threads))
+    else:
+        rc = _lib().oracle_moe_forward(*args)
+    _check(rc, "moe_forward")
     return {"y_f64": y64, "y": yo, "topk_idx": idx, "topk_w": w, "gap": gap}

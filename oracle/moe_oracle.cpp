@@ -1,7 +1,8 @@
 // Oracle for one sparse Mixture-of-Experts layer's forward pass.
 //
-// TEST INFRASTRUCTURE ONLY. This is a plain, slow, single-threaded CPU
-// statement of what the layer computes. Only the test suite, the smoke check
+// TEST INFRASTRUCTURE ONLY. This is a plain, slow CPU statement of what the
+// layer computes, on one thread (the whole-layer forward can also split its
+// token list over std::threads that run the same per-token code). Only the test suite, the smoke check
 // and the benchmark's CPU-baseline leg may load it; the product library never
 // does, and this file shares no code, header, table or helper with it.
 //
@@ -42,6 +43,7 @@
 #include <cstdint>
 #include <cstring>
 #include <limits>
+#include <thread>
 #include <vector>
 
 namespace {
@@ -192,6 +194,62 @@ bool bad_dims(int T, int d, int E, int k) {
   return T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E;
 }
 
+// The layer for list positions [i0, i1) of the token list: route and select
+// the token's k experts, then y[t] = sum_j g_j * FFN_{e_j}(x[t]) in double
+// with j ascending ([OV] section 2.1: routing, top-k, per-expert FFN, weighted
+// merge). Writes only the rows of its own positions. Returns -1 on a token
+// index outside [0, T).
+struct ForwardArgs {
+  const void *x, *w_r, *w_gate, *w_up, *w_down, *s_gate, *s_up, *s_down;
+  const float* b_r;
+  int act_dt, T, d, E, k, w_dt, f;
+  const int32_t* tokens;
+  double* y_f64;
+  void* y_out;
+  int32_t* topk_idx;
+  float* topk_w;
+  float* gap;
+};
+
+int forward_range(const ForwardArgs& A, int i0, int i1) {
+  const int d = A.d, k = A.k, f = A.f;
+  std::vector<float> l(A.E);
+  std::vector<int32_t> idx(k);
+  std::vector<float> g(k);
+  std::vector<double> yt(d), ye(d), h;
+  for (int i = i0; i < i1; ++i) {
+    const int t = A.tokens ? A.tokens[i] : i;
+    if (t < 0 || t >= A.T) return -1;
+    token_logits(A.x, A.act_dt, A.w_r, A.b_r, t, d, A.E, l.data());
+    float gp = 0.f;
+    select_one(l.data(), A.E, k, idx.data(), g.data(), &gp, nullptr);
+    for (int o = 0; o < d; ++o) yt[o] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[j];
+      const WeightView wg = expert_view(A.w_gate, A.s_gate, A.w_dt, e, f, d);
+      const WeightView wu = expert_view(A.w_up, A.s_up, A.w_dt, e, f, d);
+      const WeightView wd = expert_view(A.w_down, A.s_down, A.w_dt, e, d, f);
+      ffn_row(A.x, A.act_dt, t, d, f, wg, wu, wd, h, ye.data());
+      for (int o = 0; o < d; ++o) yt[o] += static_cast<double>(g[j]) * ye[o];
+    }
+    for (int o = 0; o < d; ++o) {
+      const size_t q = static_cast<size_t>(i) * d + o;
+      if (A.y_f64) A.y_f64[q] = yt[o];
+      if (A.y_out) {
+        const float v = static_cast<float>(yt[o]);
+        if (A.act_dt == DT_F32) static_cast<float*>(A.y_out)[q] = v;
+        else static_cast<uint16_t*>(A.y_out)[q] = float_to_bf16_rne(v);
+      }
+    }
+    if (A.topk_idx)
+      for (int j = 0; j < k; ++j) A.topk_idx[static_cast<size_t>(i) * k + j] = idx[j];
+    if (A.topk_w)
+      for (int j = 0; j < k; ++j) A.topk_w[static_cast<size_t>(i) * k + j] = g[j];
+    if (A.gap) A.gap[i] = gp;
+  }
+  return 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -300,6 +358,41 @@ int oracle_combine(const float* y_perm, const int32_t* assign_row, const float* 
   return 0;
 }
 
+// The same layer with the token list split into n_threads contiguous ranges,
+// one std::thread each. Every token is computed by the same code as in the
+// single-threaded call and written to its own rows, so the outputs are
+// bit-identical to it for any n_threads (n_threads <= 1 runs on the calling
+// thread).
+int oracle_moe_forward_mt(const void* x, int act_dt, int T, int d, const void* w_r,
+                          const float* b_r, int E, int k, const void* w_gate,
+                          const void* w_up, const void* w_down, const void* s_gate,
+                          const void* s_up, const void* s_down, int w_dt, int f,
+                          const int32_t* tokens, int n_tokens, double* y_f64,
+                          void* y_out, int32_t* topk_idx, float* topk_w, float* gap,
+                          int n_threads) {
+  if (bad_dims(T, d, E, k) || f <= 0 || !x || !w_r) return -1;
+  if (tokens && n_tokens < 0) return -1;
+  const int n = tokens ? n_tokens : T;
+  const ForwardArgs A{x,      w_r,    w_gate, w_up, w_down, s_gate, s_up, s_down, b_r,
+                      act_dt, T,      d,      E,    k,      w_dt,   f,    tokens, y_f64,
+                      y_out,  topk_idx, topk_w, gap};
+  int nt = n_threads < 1 ? 1 : n_threads;
+  if (nt > n) nt = n > 0 ? n : 1;
+  if (nt == 1) return forward_range(A, 0, n);
+  std::vector<int> rc(nt, 0);
+  std::vector<std::thread> pool;
+  pool.reserve(nt);
+  for (int w = 0; w < nt; ++w) {
+    const int i0 = static_cast<int>(static_cast<long>(n) * w / nt);
+    const int i1 = static_cast<int>(static_cast<long>(n) * (w + 1) / nt);
+    pool.emplace_back([&A, &rc, w, i0, i1] { rc[w] = forward_range(A, i0, i1); });
+  }
+  for (auto& th : pool) th.join();
+  for (int r : rc)
+    if (r != 0) return r;
+  return 0;
+}
+
 // Whole layer for the listed tokens (all T when tokens == NULL): route, select,
 // then y[t] = sum_j g_j * FFN_{e_j}(x[t]). Outputs are per listed token:
 // y_f64 [n][d] (nullable), y_out [n][d] in the act dtype (nullable),
@@ -310,41 +403,9 @@ int oracle_moe_forward(const void* x, int act_dt, int T, int d, const void* w_r,
                        const void* s_up, const void* s_down, int w_dt, int f,
                        const int32_t* tokens, int n_tokens, double* y_f64,
                        void* y_out, int32_t* topk_idx, float* topk_w, float* gap) {
-  if (bad_dims(T, d, E, k) || f <= 0 || !x || !w_r) return -1;
-  const int n = tokens ? n_tokens : T;
-  std::vector<float> l(E);
-  std::vector<int32_t> idx(k);
-  std::vector<float> g(k);
-  std::vector<double> yt(d), ye(d), h;
-  for (int i = 0; i < n; ++i) {
-    const int t = tokens ? tokens[i] : i;
-    if (t < 0 || t >= T) return -1;
-    token_logits(x, act_dt, w_r, b_r, t, d, E, l.data());
-    float gp = 0.f;
-    select_one(l.data(), E, k, idx.data(), g.data(), &gp, nullptr);
-    for (int o = 0; o < d; ++o) yt[o] = 0.0;
-    for (int j = 0; j < k; ++j) {
-      const int e = idx[j];
-      const WeightView wg = expert_view(w_gate, s_gate, w_dt, e, f, d);
-      const WeightView wu = expert_view(w_up, s_up, w_dt, e, f, d);
-      const WeightView wd = expert_view(w_down, s_down, w_dt, e, d, f);
-      ffn_row(x, act_dt, t, d, f, wg, wu, wd, h, ye.data());
-      for (int o = 0; o < d; ++o) yt[o] += static_cast<double>(g[j]) * ye[o];
-    }
-    for (int o = 0; o < d; ++o) {
-      const size_t q = static_cast<size_t>(i) * d + o;
-      if (y_f64) y_f64[q] = yt[o];
-      if (y_out) {
-        const float v = static_cast<float>(yt[o]);
-        if (act_dt == DT_F32) static_cast<float*>(y_out)[q] = v;
-        else static_cast<uint16_t*>(y_out)[q] = float_to_bf16_rne(v);
-      }
-    }
-    if (topk_idx) for (int j = 0; j < k; ++j) topk_idx[static_cast<size_t>(i) * k + j] = idx[j];
-    if (topk_w) for (int j = 0; j < k; ++j) topk_w[static_cast<size_t>(i) * k + j] = g[j];
-    if (gap) gap[i] = gp;
-  }
-  return 0;
+  return oracle_moe_forward_mt(x, act_dt, T, d, w_r, b_r, E, k, w_gate, w_up, w_down,
+                               s_gate, s_up, s_down, w_dt, f, tokens, n_tokens, y_f64,
+                               y_out, topk_idx, topk_w, gap, 1);
 }
 
 }  // extern "C"

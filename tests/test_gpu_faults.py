@@ -49,6 +49,58 @@ def test_out_of_range_expert_id_is_latched(T):
     assert np.array_equal(bufs[0].cpu().numpy(), np.bincount(good.numpy().ravel(), minlength=8))
 
 
+def test_combine_after_skipped_ids_reads_nothing_out_of_range():
+    """A bad id skipped by the dispatch leaves assign_row = -1; the combine on
+    that output adds nothing for it, latches the error and reads no row."""
+    assert moe.coli_device_status() == moe.COLI_OK
+    T, E, k, d = 40, 8, 2, 64
+    idx = inputs.random_assignments(T, E, k, seed=5)
+    idx[7, 1] = 1 << 20     # far outside [0, E)
+    rc, bufs = _permute(idx, E, k, d)
+    assert rc == moe.COLI_OK
+    assert moe.coli_device_status() == moe.COLI_EDEVICE
+    assign_row = bufs[3]
+    ar = assign_row.cpu().numpy()
+    assert ar[7 * k + 1] == -1 and (np.delete(ar, 7 * k + 1) >= 0).all()
+    y_perm = inputs.random_rows(T * k, d, inputs.F32, seed=6).cuda()
+    gates = inputs.random_gates(T, k, seed=7).cuda()
+    y = torch.empty(T, d, dtype=torch.float32, device="cuda")
+    assert moe.coli_combine(y_perm, assign_row, gates, T, k, d, moe.F32, y) == moe.COLI_OK
+    assert moe.coli_device_status() == moe.COLI_EDEVICE
+    yc = y.cpu().numpy()
+    g = gates.cpu().numpy()
+    yp = y_perm.cpu().numpy()
+    # the skipped slot contributes nothing; the other slot is there
+    assert np.allclose(yc[7], g[7, 0] * yp[ar[7 * k]], rtol=1e-6, atol=1e-7)
+    assert moe.coli_device_status() == moe.COLI_OK
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (64, 4)])
+def test_nan_router_row_still_gives_k_distinct_ids(E, k):
+    """A NaN in a token's activations makes its logits NaN: the router ranks
+    them as -inf, so the token still gets k distinct ids in [0, E), and the
+    data error is latched (both the fused E <= 32 and the E > 32 router)."""
+    assert moe.coli_device_status() == moe.COLI_OK
+    T, d = 20, 256
+    s = inputs.MoEShape("nan", T=T, d=d, E=E, k=k, f=64)
+    lay = inputs.make_layer(s, seed=8, experts=False)
+    x = lay["x"].clone()
+    x[3, 17] = float("nan")
+    xd, wr = x.cuda(), lay["w_router"].cuda()
+    idx = torch.full((T, k), -9, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    nb = moe.coli_route_scratch_bytes(T, d, E)
+    scratch = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
+    assert moe.coli_route_topk(xd, wr, None, T, d, E, k, moe.BF16, idx, w, None, scratch,
+                               nb) == moe.COLI_OK
+    assert moe.coli_device_status() == moe.COLI_EDEVICE
+    ids = idx.cpu().numpy()
+    for t in range(T):
+        assert len(set(ids[t])) == k and ids[t].min() >= 0 and ids[t].max() < E
+    assert np.isfinite(w.cpu().numpy()[np.arange(T) != 3]).all()
+    assert moe.coli_device_status() == moe.COLI_OK
+
+
 def test_bounded_wait_times_out_and_context_survives():
     assert moe.coli_device_status() == moe.COLI_OK
     assert moe.coli_selftest_bounded_wait(2000) == moe.COLI_OK

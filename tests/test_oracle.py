@@ -236,6 +236,68 @@ def test_combine_one_hot_is_gather(oracle_mod):
     assert np.array_equal(yb, _bits(torch.from_numpy(y_perm[perm]).to(torch.bfloat16)))
 
 
+def test_combine_k2_k3_hand_computed(oracle_mod):
+    """The weighted merge y[t] = sum_j g[t][j] * y_perm[assign_row[t*k+j]] on
+    values worked out by hand (gates and rows exact in binary, so the expected
+    outputs are exact): a transposed gather index, a swapped gate or a dropped
+    slot each change at least one of them."""
+    # k = 2, T = 2, d = 3; assign_row sends token 0 to rows (2, 0), token 1 to (1, 3)
+    y_perm = np.array([[4.0, -8.0, 1.0],
+                       [2.0, 6.0, -2.0],
+                       [-4.0, 0.5, 8.0],
+                       [16.0, -1.0, 0.0]], np.float32)
+    assign = np.array([2, 0, 1, 3], np.int32)
+    gates = np.array([[0.75, 0.25], [0.5, 0.5]], np.float32)
+    # token 0: 0.75*(-4, 0.5, 8) + 0.25*(4, -8, 1) = (-3+1, 0.375-2, 6+0.25)
+    # token 1: 0.5*(2, 6, -2) + 0.5*(16, -1, 0)     = (1+8, 3-0.5, -1+0)
+    want = np.array([[-2.0, -1.625, 6.25], [9.0, 2.5, -1.0]])
+    y64, yo = oracle_mod.combine(y_perm, assign, gates, 2, 2, 3, inputs.F32)
+    assert np.array_equal(y64, want) and np.array_equal(yo, want.astype(np.float32))
+    # k = 3, T = 1, d = 2; slots read rows 1, 2, 0 with gates 1/2, 1/4, 1/4
+    y_perm = np.array([[8.0, 1.0], [2.0, -4.0], [-16.0, 3.0]], np.float32)
+    assign = np.array([1, 2, 0], np.int32)
+    gates = np.array([[0.5, 0.25, 0.25]], np.float32)
+    # 0.5*(2, -4) + 0.25*(-16, 3) + 0.25*(8, 1) = (1-4+2, -2+0.75+0.25)
+    want = np.array([[-1.0, -1.0]])
+    y64, yo = oracle_mod.combine(y_perm, assign, gates, 1, 3, 2, inputs.F32)
+    assert np.array_equal(y64, want) and np.array_equal(yo, want.astype(np.float32))
+    # bf16 output: 0.5*1 + 0.5*(1 + 2^-8) = 1 + 2^-9, halfway between the bf16
+    # values 1 and 1 + 2^-7: round to nearest even gives 1.0 (0x3F80); and
+    # 0.5*(1 + 2^-7) + 0.5*(1 + 2^-6) = 1 + 3*2^-8 rounds up to 1 + 2^-6 (0x3F82)
+    y_perm = np.array([[1.0, 1 + 2.0 ** -7], [1 + 2.0 ** -8, 1 + 2.0 ** -6]], np.float32)
+    assign = np.array([0, 1], np.int32)
+    gates = np.array([[0.5, 0.5]], np.float32)
+    y64, yb = oracle_mod.combine(y_perm, assign, gates, 1, 2, 2, inputs.BF16)
+    assert np.array_equal(y64, [[1 + 2.0 ** -9, 1 + 3 * 2.0 ** -8]])
+    assert yb.tolist() == [[0x3F80, 0x3F82]]
+
+
+@pytest.mark.parametrize("act,wdt,bias", [("bf16", "bf16", "zipf"), ("f32", "f32", "none"),
+                                          ("bf16", "i4g128", "none")])
+def test_threaded_forward_is_bit_identical(oracle_mod, act, wdt, bias):
+    """The N-thread forward (token list split over std::threads) returns the
+    single-threaded call's bits for every thread count, with and without a
+    token list, including more threads than tokens."""
+    s = inputs.MoEShape("mt", T=23, d=256, E=8, k=3, f=128, act=act, wdt=wdt, bias=bias)
+    lay = inputs.make_layer(s, seed=17)
+    one = oracle_mod.moe_forward(lay, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f)
+    for n in (2, 3, 7, 40):
+        many = oracle_mod.moe_forward(lay, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f,
+                                      threads=n)
+        for key in one:
+            assert np.array_equal(one[key], many[key]), (n, key)
+    tok = [5, 0, 22, 5, 11]
+    sub1 = oracle_mod.moe_forward(lay, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f, tokens=tok)
+    sub4 = oracle_mod.moe_forward(lay, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f, tokens=tok,
+                                  threads=4)
+    for key in sub1:
+        assert np.array_equal(sub1[key], sub4[key]), key
+    assert np.array_equal(sub1["y_f64"], one["y_f64"][tok])
+    with pytest.raises(ValueError):
+        oracle_mod.moe_forward(lay, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f,
+                               tokens=[0, 23], threads=2)
+
+
 def test_forward_equals_staged_composition(oracle_mod):
     s = inputs.MoEShape("mini", T=20, d=128, E=6, k=3, f=64, act="bf16", wdt="bf16")
     lay = inputs.make_layer(s, seed=16)

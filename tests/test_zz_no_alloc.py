@@ -66,6 +66,29 @@ def test_noalloc_matches_coli_permute_on_two_calls_in_a_row():
         assert moe.coli_device_status() == moe.COLI_OK
 
 
+@pytest.mark.parametrize("T,E,k", [
+    (2048, 64, 8),     # 16384 assignments: the single-block path, no table
+    (16384, 256, 8),   # 64 blocks x 256 experts x 4 B = exactly the 65536-byte area
+    (131072, 64, 4),   # 524288 assignments at E = 64: 256 blocks x 64 x 4 B, also exactly full
+])
+def test_noalloc_boundary_shapes(T, E, k):
+    """The path that needs no table, and the two largest batches whose table
+    fills the area exactly: bit-exact against coli_permute with caller scratch."""
+    d = 64
+    need = moe.coli_permute_scratch_bytes(T, k, E)
+    assert need <= moe.COLI_PERMUTE_STATIC_SCRATCH_BYTES
+    if T * k > 16384:
+        assert need == moe.COLI_PERMUTE_STATIC_SCRATCH_BYTES
+    idx = inputs.random_assignments(T, E, k, seed=T % 97).cuda()
+    x = inputs.random_rows(T, d, moe.BF16, seed=3).cuda()
+    ref = _with_caller_scratch(idx, x, T, d, E, k, moe.BF16)
+    got = _without_scratch(idx, x, T, d, E, k, moe.BF16)
+    torch.cuda.synchronize()
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+    assert moe.coli_device_status() == moe.COLI_OK
+
+
 def test_noalloc_rejects_batches_beyond_its_area():
     T, k, E = 16385, 8, 256  # needs 65 blocks x 256 experts x 4 bytes > 65536
     assert moe.coli_permute_scratch_bytes(T, k, E) > moe.COLI_PERMUTE_STATIC_SCRATCH_BYTES
@@ -74,3 +97,13 @@ def test_noalloc_rejects_batches_beyond_its_area():
                                   fake)
     assert rc == moe.COLI_EINVAL
     assert "static" in moe.last_error()
+    # one row past the E = 64 limit as well
+    T, k, E = 131073, 4, 64
+    assert moe.coli_permute_scratch_bytes(T, k, E) > moe.COLI_PERMUTE_STATIC_SCRATCH_BYTES
+    rc = moe.coli_permute_noalloc(fake, fake, T, 64, E, k, moe.BF16, fake, fake, fake, fake,
+                                  fake)
+    assert rc == moe.COLI_EINVAL
+    # a size outside the general limits names the sizes and the T*k bound
+    rc = moe.coli_permute_noalloc(fake, fake, 1 << 22, 64, 8, 8, moe.BF16, fake, fake, fake,
+                                  fake, fake)
+    assert rc == moe.COLI_EINVAL and "16777216" in moe.last_error()
