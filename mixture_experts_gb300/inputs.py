@@ -8,7 +8,10 @@ tensors produced here.
 Recipe (fixed so every run of every consumer sees the same bits):
 
 * ``torch.Generator().manual_seed(seed)`` on the CPU, fp32 draws in the order
-  x, W_r, b_r, then for each expert e = 0..E-1: W_gate[e], W_up[e], W_down[e].
+  x, W_r, b_r. Expert e = 0..E-1 has a generator of its own,
+  ``manual_seed(expert_seed(seed, e))``, drawing W_gate[e], W_up[e], W_down[e]
+  in that order; so the experts can be drawn in parallel threads and the bits
+  do not depend on how many threads there are.
 * x ~ N(0, 1); every weight ~ N(0, 0.02). Weights are drawn directly in the
   ``[out][in]`` layout (reduction index contiguous): W_r [E][d], gate/up
   [E][f][d], down [E][d][f].
@@ -27,6 +30,8 @@ Recipe (fixed so every run of every consumer sees the same bits):
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, replace
 
 import torch
@@ -108,6 +113,25 @@ def zipf_bias(E: int, alpha: float, perm: torch.Tensor, s: float = ZIPF_S) -> to
     return (alpha * logp[perm.long()]).to(torch.float32)
 
 
+def expert_seed(seed: int, e: int) -> int:
+    """Seed of expert e's own generator (distinct for e < 2^20)."""
+    return (seed << 20) + 1 + e
+
+
+def _draw_experts(E: int, seed: int, one):
+    """one(e, generator) for every expert, in parallel threads (torch ops
+    release the interpreter lock); each expert has its own seeded generator."""
+    def job(e):
+        one(e, torch.Generator().manual_seed(expert_seed(seed, e)))
+    workers = max(1, min(E, os.cpu_count() or 1, 32))
+    if workers == 1:
+        for e in range(E):
+            job(e)
+        return
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(job, range(E)))
+
+
 def make_layer(shape: MoEShape, seed: int = 0, experts: bool = True) -> dict:
     """All inputs of one layer as CPU tensors in the canonical layouts.
 
@@ -138,20 +162,22 @@ def make_layer(shape: MoEShape, seed: int = 0, experts: bool = True) -> dict:
         sg = torch.empty(E, f, d // GROUP, dtype=torch.bfloat16)
         su = torch.empty(E, f, d // GROUP, dtype=torch.bfloat16)
         sd = torch.empty(E, d, f // GROUP, dtype=torch.bfloat16)
-        for e in range(E):
-            wg[e], sg[e] = quantize_i4g128(torch.randn(f, d, generator=g) * 0.02)
-            wu[e], su[e] = quantize_i4g128(torch.randn(f, d, generator=g) * 0.02)
-            wd[e], sd[e] = quantize_i4g128(torch.randn(d, f, generator=g) * 0.02)
+        def one(e, ge):
+            wg[e], sg[e] = quantize_i4g128(torch.randn(f, d, generator=ge) * 0.02)
+            wu[e], su[e] = quantize_i4g128(torch.randn(f, d, generator=ge) * 0.02)
+            wd[e], sd[e] = quantize_i4g128(torch.randn(d, f, generator=ge) * 0.02)
+        _draw_experts(E, seed, one)
         out.update(w_gate=wg, w_up=wu, w_down=wd, s_gate=sg, s_up=su, s_down=sd)
     else:
         dt = torch.float32 if shape.w_code == F32 else torch.bfloat16
         wg = torch.empty(E, f, d, dtype=dt)
         wu = torch.empty(E, f, d, dtype=dt)
         wd = torch.empty(E, d, f, dtype=dt)
-        for e in range(E):
-            wg[e] = torch.randn(f, d, generator=g) * 0.02
-            wu[e] = torch.randn(f, d, generator=g) * 0.02
-            wd[e] = torch.randn(d, f, generator=g) * 0.02
+        def one(e, ge):
+            wg[e] = torch.randn(f, d, generator=ge) * 0.02
+            wu[e] = torch.randn(f, d, generator=ge) * 0.02
+            wd[e] = torch.randn(d, f, generator=ge) * 0.02
+        _draw_experts(E, seed, one)
         out.update(w_gate=wg, w_up=wu, w_down=wd, s_gate=None, s_up=None, s_down=None)
     return out
 
