@@ -1,8 +1,11 @@
 """Benchmark of one sparse MoE layer forward on GB300.
 
-Default workload: the Mixtral-8x7B-shaped layer at a decode batch (T=32,
+Headline workload: the Mixtral-8x7B-shaped layer at a decode batch (T=32,
 d=4096, E=8, k=2, d_ff=14336, bf16), whose expert FFN streams the 2.8 GB of
-activated expert weights once per forward. Prints ONE JSON line (rank 0).
+activated expert weights once per forward. At N=1 a default run also measures
+the other workloads (prefill, int4, skewed, fp32) and reports each under the
+line's "configs" key with its own roofline, stage split, clocks and oracle
+sample. Prints ONE JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
     python bench.py --impl reference ...   # the CPU oracle on a bounded sample
@@ -44,7 +47,11 @@ def parse():
                         "--steps and --warmup are")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="budget of the oracle CPU-baseline sample")
+    p.add_argument("--sub-cpu-seconds", type=float, default=6.0,
+                   help="budget of the oracle sample of each non-headline workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--headline-only", action="store_true",
+                   help="measure only --config (default: also every other workload, at N=1)")
     p.add_argument("--experts", type=int, default=0,
                    help="profiling aid: keep the per-expert shapes but use this many experts "
                         "(and T scaled to keep the rows per expert)")
@@ -286,22 +293,76 @@ def traffic_record(config: str, kind: str):
 
 
 # ---------------------------------------------------------------- GPU leg
-def run_coli(args):
-    import numpy as np
+def roofline(s, path, n_rows, active, avg, ms_fwd, pk, pk_src, config_name):
+    """Dominant kernel's roofline (gate/up projection: the decode weight
+    stream or the prefill grouped GEMM) plus whole-layer figures."""
+    gu_ms = avg[2]
+    ffn_ms = avg[2] + avg[3]
+    if path == "decode":
+        if s.wdt == "i4g128":
+            per_expert = 2 * s.f * s.d // 2 + 2 * s.f * (s.d // 128) * 2
+            all_bytes = active * (3 * s.f * s.d // 2 + 3 * s.f * (s.d // 128) * 2)
+        else:
+            wsz = 4 if s.wdt == "f32" else 2
+            per_expert = 2 * s.f * s.d * wsz
+            all_bytes = active * 3 * s.f * s.d * wsz
+        alg = per_expert * active
+        achieved = alg / (gu_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"],
+                "traffic": traffic_record(config_name, "dec"),
+                "kernel": "k_dec_gateup (expert gate/up projection + SwiGLU)",
+                "algorithmic_bytes_per_launch": alg,
+                "unit_work": f"{per_expert} B of gate/up weights per activated expert x "
+                             f"{active} activated experts",
+                "peak_source": f"{pk_src} hbm_gbs"}
+        roof["expert_ffn_total"] = {
+            "bytes": all_bytes, "achieved_gbs": all_bytes / (ffn_ms / 1e3) / 1e9,
+            "frac": all_bytes / (ffn_ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+        # the layer's figure: activated-expert weight bytes over the whole forward
+        roof["layer"] = {"achieved_gbs": all_bytes / (ms_fwd / 1e3) / 1e9,
+                         "frac": all_bytes / (ms_fwd / 1e3) / 1e9 / pk["hbm_gbs"]}
+    else:
+        flops = 2.0 * n_rows * s.d * 2 * s.f
+        achieved = flops / (gu_ms / 1e3) / 1e12
+        burst = pk["bf16_tflops"]
+        sust = pk.get("bf16_tflops_sustained", burst)
+        roof = {"bound": "tensor", "achieved": achieved, "peak": sust, "unit": "TFLOP/s",
+                "frac": achieved / sust, "frac_burst": achieved / burst,
+                "frac_sustained": achieved / sust,
+                "traffic": traffic_record(config_name, "tc"),
+                "kernel": "k_tc_gemm (gate/up grouped GEMM + SwiGLU)",
+                "algorithmic_flops_per_launch": flops,
+                "unit_work": f"2 x {n_rows} rows x d={s.d} x 2f={2 * s.f} FLOP",
+                "peak_source": f"{pk_src} bf16_tflops_sustained (burst {burst})"}
+        dn_flops = 2.0 * n_rows * s.f * s.d
+        dn = dn_flops / (avg[3] / 1e3) / 1e12
+        roof["down_gemm"] = {"achieved": dn, "frac_burst": dn / burst, "frac_sustained": dn / sust}
+        layer_flops = 2.0 * n_rows * 3 * s.d * s.f
+        lay = layer_flops / (ms_fwd / 1e3) / 1e12
+        roof["layer"] = {"flops": layer_flops, "achieved_tflops": lay, "frac_burst": lay / burst,
+                         "frac_sustained": lay / sust}
+    # intermediates are not algorithmic bytes: x_perm (written by dispatch,
+    # read by gate/up), H (written and read), y_perm (fp32, written by down,
+    # read by combine), listed separately per forward; the decode path with
+    # bf16/int4 experts reads token rows of x directly and writes no x_perm
+    asz = 4 if s.act == "f32" else 2
+    xperm = 0 if (path == "decode" and s.wdt != "f32") else 2 * n_rows * s.d * asz
+    roof["overhead_bytes"] = {
+        "x_perm": xperm, "H": 2 * n_rows * s.f * (4 if s.wdt == "f32" else 2),
+        "y_perm": 2 * n_rows * s.d * 4}
+    return roof
+
+
+def measure(s, steps, warmup, world, rank, local, cpu_seconds, with_e2e=True,
+            config_name=None):
+    """Times `steps` forwards of workload `s` (inputs resident in HBM) and
+    returns the per-workload record: value, stage split, roofline, clocks,
+    end-to-end figure through the host-buffer API and the oracle sample."""
     import torch
     import mixture_experts_gb300 as moe
     from mixture_experts_gb300 import inputs
 
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    moe.build()
-    s = inputs.CONFIGS[args.config]
-    if args.experts:
-        s = s.with_(name=f"{s.name}[E={args.experts}]", E=args.experts,
-                    T=max(1, s.T * args.experts // s.E), k=min(s.k, args.experts))
     host = inputs.make_layer(s, seed=0)
     if rank > 0:  # replicas: same weights, this rank's own tokens
         host["x"] = inputs.random_rows(s.T, s.d, s.act_code, seed=1000 + rank)
@@ -324,7 +385,7 @@ def run_coli(args):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         layer(x, y)
     barrier()
 
@@ -340,7 +401,7 @@ def run_coli(args):
 
     # clocks are sampled under load only: the sampler starts while untimed
     # forwards run, and a timed region shorter than the sampling needs is
-    # followed by more of them (stated in the line's clocks.window)
+    # followed by more of them (stated in the record's clocks.window)
     clocks = ClockSampler(local)
     clocks.start()
     pre = busy(0.5)
@@ -352,7 +413,7 @@ def run_coli(args):
     barrier()
     if flush:
         per = []
-        for _ in range(args.steps):
+        for _ in range(steps):
             scrub.zero_()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
@@ -366,7 +427,7 @@ def run_coli(args):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             layer(x, y)
         b.record(stream)
         barrier()
@@ -379,108 +440,127 @@ def run_coli(args):
     clk["window"] = (f"{pre} untimed forwards while the sampler started, the timed region"
                      + (f", then {post} more untimed forwards (the timed region lasted "
                         f"{elapsed_ms:.1f} ms)" if post else ""))
-    tokens, seconds = aggregate(s.T * args.steps, elapsed_ms / 1e3, world)
+    tokens, seconds = aggregate(s.T * steps, elapsed_ms / 1e3, world)
     value = tokens / seconds
 
-    # ---- dominant kernel roofline
     pk, pk_src = peaks()
     dbg = layer.debug(s.T)
     counts = dbg["counts"].cpu().numpy()
     active = int((counts > 0).sum())
     n_rows = int(counts.sum())
     avg = [m / max(1, n_fwd) for m in stage_ms]
-    gu_ms = avg[2]
-    if path == "decode":
-        if s.wdt == "i4g128":
-            per_expert = 2 * s.f * s.d // 2 + 2 * s.f * (s.d // 128) * 2
-        else:
-            per_expert = 2 * s.f * s.d * (4 if s.wdt == "f32" else 2)
-        alg = per_expert * active
-        achieved = alg / (gu_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"],
-                "traffic": traffic_record(args.config, "dec"),
-                "kernel": "k_dec_gateup (expert gate/up projection + SwiGLU)",
-                "algorithmic_bytes_per_launch": alg,
-                "unit_work": f"{per_expert} B of gate/up weights per activated expert x "
-                             f"{active} activated experts",
-                "peak_source": f"{pk_src} hbm_gbs"}
-    else:
-        flops = 2.0 * n_rows * s.d * 2 * s.f
-        achieved = flops / (gu_ms / 1e3) / 1e12
-        peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic_record(args.config, "tc"),
-                "kernel": "k_tc_gemm (gate/up grouped GEMM + SwiGLU)",
-                "algorithmic_flops_per_launch": flops,
-                "peak_source": f"{pk_src} bf16_tflops_sustained"}
-    ffn_ms = avg[2] + avg[3]
-    # intermediates are not algorithmic bytes: x_perm (written by dispatch,
-    # read by gate/up), H (bf16, written and read), y_perm (fp32, written by
-    # down, read by combine); listed separately per forward
-    # (the decode path with bf16/int4 experts reads token rows of x directly
-    # and writes no x_perm)
-    asz = 4 if s.act == "f32" else 2
-    xperm = 0 if (path == "decode" and s.wdt != "f32") else 2 * n_rows * s.d * asz
-    roof["overhead_bytes"] = {
-        "x_perm": xperm, "H": 2 * n_rows * s.f * (4 if s.wdt == "f32" else 2),
-        "y_perm": 2 * n_rows * s.d * 4}
-    if path == "decode":
-        if s.wdt == "i4g128":
-            all_bytes = active * (3 * s.f * s.d // 2 + 3 * s.f * (s.d // 128) * 2)
-        else:
-            all_bytes = active * 3 * s.f * s.d * 2
-        roof["expert_ffn_total"] = {"achieved_gbs": all_bytes / (ffn_ms / 1e3) / 1e9,
-                                    "frac": all_bytes / (ffn_ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+    roof = roofline(s, path, n_rows, active, avg, elapsed_ms / steps, pk, pk_src,
+                    config_name or s.name)
 
-    # ---- end to end through the public API with host buffers
-    xh = host["x"].pin_memory()
-    yh = torch.empty_like(xh).pin_memory()
-    for _ in range(3):
-        layer.forward_host(xh, yh)
-    e2e_steps = max(10, min(args.steps, 500))
-    barrier()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        layer.forward_host(xh, yh)
-    e2e_s = time.perf_counter() - t0
-    e_tokens, e_seconds = aggregate(s.T * e2e_steps, e2e_s, world)
-    io_bytes = s.T * s.d * (4 if s.act == "f32" else 2)
+    rec = {"workload": workload_desc(s), "path": path, "value": value, "unit": "tokens/s",
+           "steps": steps, "warmup": max(3, warmup), "ms_per_step": elapsed_ms / steps,
+           "l2": ("L2 flushed between steps" if flush else
+                  f"inputs larger than L2: {weight_bytes / 1e9:.2f} GB of expert weights "
+                  f"streamed per step"),
+           "active_experts": active, "roofline": roof,
+           "stage_ms": dict(zip(STAGES, [round(m, 5) for m in avg])),
+           "gpu_launches": int(n_launch * steps / max(1, n_fwd)), "clocks": clk}
+
+    if with_e2e:
+        # end to end through the public API with host buffers (pinned)
+        xh = host["x"].pin_memory()
+        yh = torch.empty_like(xh).pin_memory()
+        for _ in range(3):
+            layer.forward_host(xh, yh)
+        e2e_steps = max(10, min(steps, 500))
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            layer.forward_host(xh, yh)
+        e2e_s = time.perf_counter() - t0
+        e_tokens, e_seconds = aggregate(s.T * e2e_steps, e2e_s, world)
+        io_bytes = s.T * s.d * (4 if s.act == "f32" else 2)
+        rec["e2e"] = {"value": e_tokens / e_seconds, "unit": "tokens/s",
+                      "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes}
+    layer.close()
+    del x, y, scrub
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and cpu_seconds > 0:
+        tps, n, dt = oracle_sample(s, host, cpu_seconds)
+        rec["cpu_baseline"] = {
+            "value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} of the {s.T} tokens of one step, whole layer per token "
+                      f"({dt:.1f} s, one thread)",
+            "host": host_desc()}
+    else:
+        rec["cpu_baseline"] = None
+    return rec
+
+
+# the other workloads measured beside the headline one in a default run:
+# the remaining configurations, then one int4 layer at a prefill batch
+EXTRA = ["mixtral_prefill", "fine_int4", "skewed", "tiny_fp32"]
+
+
+def sub_steps(s, K: int) -> int:
+    """Timed forwards for a non-headline workload: at least K, and enough
+    for about 0.3 s of timed work (capped), from a rough cost model."""
+    flops = 2.0 * s.T * s.k * 3 * s.d * s.f
+    est_ms = max(0.02, flops / 1.2e15 * 1e3, 3 * s.d * s.f * min(s.E, s.T * s.k) *
+                 (0.53 if s.wdt == "i4g128" else 2.0) / 5.0e12 * 1e3)
+    return int(max(K, min(400, 300.0 / est_ms)))
+
+
+def run_coli(args):
+    import torch
+    import mixture_experts_gb300 as moe
+    from mixture_experts_gb300 import inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    moe.build()
+    s = inputs.CONFIGS[args.config]
+    if args.experts:
+        s = s.with_(name=f"{s.name}[E={args.experts}]", E=args.experts,
+                    T=max(1, s.T * args.experts // s.E), k=min(s.k, args.experts))
+    cpu_s = 0 if (args.no_cpu_baseline or world > 1) else args.cpu_seconds
+    head = measure(s, args.steps, args.warmup, world, rank, local, cpu_s,
+                   config_name=args.config)
+
+    others = {}
+    if world == 1 and not args.headline_only and not args.experts:
+        for name in EXTRA:
+            if name == args.config:
+                continue
+            so = inputs.CONFIGS[name]
+            rec = measure(so, sub_steps(so, args.steps), args.warmup, world, rank, local,
+                          0 if args.no_cpu_baseline else args.sub_cpu_seconds, with_e2e=False,
+                          config_name=name)
+            rec.pop("e2e", None)
+            others[name] = rec
 
     line = None
     if rank == 0:
-        cpu = None
-        if not args.no_cpu_baseline and world == 1:
-            tps, n, dt = oracle_sample(s, host, args.cpu_seconds)
-            cpu = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                   "sample": f"{n} of the {s.T} tokens of one step, whole layer per token "
-                             f"({dt:.1f} s, one thread)",
-                   "host": host_desc()}
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if s.act == "bf16" else "f32",
+            "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if s.act == "bf16" else "f32",
             "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
-            "config": {"workload": workload_desc(s), "path": path,
-                       "parallelism": f"replicas x{world}",
-                       "l2": ("L2 flushed between steps" if flush else
-                              f"inputs larger than L2: {weight_bytes / 1e9:.2f} GB of expert "
-                              f"weights streamed per step"),
-                       "active_experts": active},
-            "roofline": roof,
-            "stage_ms": dict(zip(STAGES, [round(m, 5) for m in avg])),
-            "cpu_baseline": cpu,
-            "e2e": {"value": e_tokens / e_seconds, "unit": "tokens/s",
-                    "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes},
-            "gpu_launches": int(n_launch * args.steps / max(1, n_fwd)),
-            "clocks": clk,
+            "config": {"workload": head["workload"], "path": head["path"],
+                       "parallelism": f"replicas x{world}", "l2": head["l2"],
+                       "active_experts": head["active_experts"]},
+            "roofline": head["roofline"],
+            "stage_ms": head["stage_ms"],
+            "cpu_baseline": head["cpu_baseline"],
+            "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"],
+            "clocks": head["clocks"],
         }
+        if others:
+            line["configs"] = others
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
-    layer.close()
     return line
 
 
