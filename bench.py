@@ -331,7 +331,9 @@ def roofline(s, path, n_rows, active, avg, ms_fwd, pk, pk_src, config_name):
                 "frac": achieved / sust, "frac_burst": achieved / burst,
                 "frac_sustained": achieved / sust,
                 "traffic": traffic_record(config_name, "tc"),
-                "kernel": "k_tc_gemm (gate/up grouped GEMM + SwiGLU)",
+                "kernel": ("k_tc_gemm<int4> (gate/up grouped GEMM, int4 weights dequantised "
+                           "to bf16 in shared memory, + SwiGLU)" if s.wdt == "i4g128" else
+                           "k_tc_gemm (gate/up grouped GEMM + SwiGLU)"),
                 "algorithmic_flops_per_launch": flops,
                 "unit_work": f"2 x {n_rows} rows x d={s.d} x 2f={2 * s.f} FLOP",
                 "peak_source": f"{pk_src} bf16_tflops_sustained (burst {burst})"}
@@ -494,7 +496,7 @@ def measure(s, steps, warmup, world, rank, local, cpu_seconds, with_e2e=True,
 
 # the other workloads measured beside the headline one in a default run:
 # the remaining configurations, then one int4 layer at a prefill batch
-EXTRA = ["mixtral_prefill", "fine_int4", "skewed", "tiny_fp32"]
+EXTRA = ["mixtral_prefill", "fine_int4", "skewed", "tiny_fp32", "mixtral_prefill_int4"]
 
 
 def sub_steps(s, K: int) -> int:

@@ -67,8 +67,12 @@ typedef enum { COLI_F32 = 0, COLI_BF16 = 1, COLI_I4G128 = 2 } coli_dtype;
  * (T*k/E) is at most 64, else PREFILL. DECODE streams each active expert's
  * weights once (tensor-core MMA fed straight from HBM); PREFILL is the
  * TMA + tcgen05/TMEM grouped GEMM. Both give the same routing and the same
- * outputs within rounding. F32 layers always use the CUDA-core path; int4
- * experts always use DECODE. */
+ * outputs within rounding. F32 layers always use the CUDA-core path.
+ * int4 experts run on both: DECODE applies each group's scale to the exact
+ * sum of q*x in fp32 (w = q*s exactly); PREFILL dequantises each weight to a
+ * bf16 tensor-core operand, q*s rounded once to nearest even (q*s can need 11
+ * significant bits, bf16 holds 8: a relative change of at most 2^-9 per
+ * weight). */
 typedef enum { COLI_PATH_AUTO = 0, COLI_PATH_DECODE = 1, COLI_PATH_PREFILL = 2 } coli_path;
 
 typedef struct {

@@ -186,7 +186,6 @@ int validate_cfg(const coli_moe_config* c, char* err, size_t err_len) {
 int pick_path(const coli_moe* h, int T) {
   const auto& c = h->cfg;
   if (c.weight_dtype == COLI_F32) return COLI_PATH_DECODE;  // CUDA-core fp32 path
-  if (c.weight_dtype == COLI_I4G128) return COLI_PATH_DECODE;
   if (h->tc == nullptr) return COLI_PATH_DECODE;
   if (c.path != COLI_PATH_AUTO) return c.path;
   return static_cast<long>(T) * c.top_k <= 64L * c.n_experts ? COLI_PATH_DECODE
@@ -399,9 +398,9 @@ int coli_moe_create(const coli_moe_config* cfg, const coli_moe_weights* wts, voi
   h->w.w_dn = wdn;
   h->w.s_gu = static_cast<const __nv_bfloat16*>(sgu);
   h->w.s_dn = static_cast<const __nv_bfloat16*>(sdn);
-  if (cfg->weight_dtype == COLI_BF16 && tc_supported(d, f)) {
-    if ((e = tc_plan_create(&h->tc, wgu, wdn, E, d, f, static_cast<int>(Na), h->x_perm,
-                            h->H)) != cudaSuccess)
+  if (cfg->weight_dtype != COLI_F32 && tc_supported(d, f)) {
+    if ((e = tc_plan_create(&h->tc, cfg->weight_dtype, wgu, wdn, h->w.s_gu, h->w.s_dn, E, d, f,
+                            static_cast<int>(Na), h->x_perm, h->H)) != cudaSuccess)
       return bail(COLI_ECUDA, "tensor-core plan", e);
   }
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return bail(COLI_ECUDA, "create sync", e);

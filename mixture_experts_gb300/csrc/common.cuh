@@ -136,6 +136,38 @@ COLI_DEV bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns = kWa
   }
 }
 
+// ---- int4 -> bf16 ------------------------------------------------------------
+// int4 -> bf16 without an offset subtraction. A repacked word holds the 8
+// indices 8w..8w+7 with even ones in nibbles 0-3 and odd ones in 4-7, so
+// nibbles (p, p+4) are the consecutive pair (2p, 2p+1). One LOP3 per pair
+// flips the nibble's sign bit and drops it into the low mantissa bits of a
+// bf16 whose exponent makes the value exactly 136 + q:
+//   ((w >> 4p) & 0x000F000F) ^ 0x43084308  ->  bf16x2 (136 + q_2p, 136 + q_2p+1)
+// The decode MMA thus sums (136 + q) x and subtracts 136 * sum(x) over the
+// group (a per-token table) to leave the exact sum q x; the prefill
+// converter subtracts the 136 from the bf16 values instead.
+COLI_DEV uint32_t nib_pair136(uint32_t w, int p) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(w >> (4 * p)), "r"(0x000F000Fu),
+      "r"(0x43084308u));
+  return r;  // (v & mask) ^ x
+}
+
+COLI_DEV uint4 dequant136(uint32_t w) {
+  return make_uint4(nib_pair136(w, 0), nib_pair136(w, 1), nib_pair136(w, 2), nib_pair136(w, 3));
+}
+
+COLI_DEV uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// bf16x2 a * b + c, one rounding per half (round to nearest even).
+COLI_DEV uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
 COLI_DEV uint32_t lane_id() { return threadIdx.x & 31u; }
 
 }  // namespace coli

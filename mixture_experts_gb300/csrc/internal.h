@@ -75,14 +75,18 @@ cudaError_t launch_f32_ffn(const float* w_gu, const float* w_dn, const float* x_
                            const int32_t* offsets, int n_rows, int E, int d, int f, float* H,
                            float* y_perm, cudaStream_t st, int* n_launches);
 
-// Prefill path: TMA + tcgen05/TMEM grouped GEMM (bf16 weights).
+// Prefill path: TMA + tcgen05/TMEM grouped GEMM (bf16 or int4 weights).
 struct TcPlan;  // defined in k_ffn_tc.cu
 bool tc_supported(int d, int f);
 // x_perm [max_rows][d] and H [max_rows][f] are the handle's buffers: their
 // tensor maps are encoded once here (rows past a forward's last group are
 // computed from stale data but never stored).
-cudaError_t tc_plan_create(TcPlan** plan, const void* w_gu, const void* w_dn, int E, int d, int f,
-                           int max_rows, const void* x_perm, const void* H);
+// wdt DT_BF16: w_gu/w_dn bf16 in the handle layout; DT_I4G128: int4 bytes
+// plus bf16 scales s_gu/s_dn (rounded to bf16 per weight when dequantised
+// for the tensor cores).
+cudaError_t tc_plan_create(TcPlan** plan, int wdt, const void* w_gu, const void* w_dn,
+                           const __nv_bfloat16* s_gu, const __nv_bfloat16* s_dn, int E, int d,
+                           int f, int max_rows, const void* x_perm, const void* H);
 void tc_plan_destroy(TcPlan* plan);
 // H[rows][f] = silu(x_perm Wg^T) * (x_perm Wu^T) per expert group (bf16).
 // own_x_perm: x_perm is the plan's buffer (its map is reused), else a map is

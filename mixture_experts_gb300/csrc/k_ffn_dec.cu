@@ -51,30 +51,6 @@ extern __shared__ __align__(16) uint8_t dec_smem[];
 
 COLI_DEV uint4 zero4() { return make_uint4(0u, 0u, 0u, 0u); }
 
-// int4 -> bf16 without an offset subtraction. A repacked word holds the 8
-// indices 8w..8w+7 with even ones in nibbles 0-3 and odd ones in 4-7, so
-// nibbles (p, p+4) are the consecutive pair (2p, 2p+1). One LOP3 per pair
-// flips the nibble's sign bit and drops it into the low mantissa bits of a
-// bf16 whose exponent makes the value exactly 136 + q:
-//   ((w >> 4p) & 0x000F000F) ^ 0x43084308  ->  bf16x2 (136 + q_2p, 136 + q_2p+1)
-// The MMA thus sums (136 + q) x; subtracting 136 * sum(x) over the group
-// (a per-token table, see k_group_sums) leaves the exact sum q x of the
-// stored weights.
-COLI_DEV uint32_t nib_pair136(uint32_t w, int p) {
-  uint32_t r;
-  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(r) : "r"(w >> (4 * p)), "r"(0x000F000Fu),
-      "r"(0x43084308u));
-  return r;  // (v & mask) ^ x
-}
-
-COLI_DEV uint4 dequant136(uint32_t w) {
-  return make_uint4(nib_pair136(w, 0), nib_pair136(w, 1), nib_pair136(w, 2), nib_pair136(w, 3));
-}
-
-COLI_DEV uint32_t word_of(const uint4& v, int i) {
-  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
-}
-
 // acc[m][n] += A(tile m) x B(n) over one 8-index chunk held as bf16 uint4s:
 // ar/ar8 rows r and r+8 of tile m, b the token fragment.
 template <int NT>

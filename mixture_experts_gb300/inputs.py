@@ -77,13 +77,18 @@ class MoEShape:
 
 # The five workloads: a tiny fp32 layer; a Mixtral-8x7B-shaped layer at a
 # decode batch and at prefill (8 sequences x 512 tokens); a fine-grained
-# 256-expert layer with int4 experts; a skewed-routing stress layer.
+# 256-expert layer with int4 experts; a skewed-routing stress layer. One more
+# measures int4 experts at a prefill batch.
 CONFIGS = {
     "tiny_fp32": MoEShape("tiny_fp32", T=64, d=256, E=8, k=2, f=512, act="f32", wdt="f32"),
     "mixtral_decode": MoEShape("mixtral_decode", T=32, d=4096, E=8, k=2, f=14336),
     "mixtral_prefill": MoEShape("mixtral_prefill", T=4096, d=4096, E=8, k=2, f=14336),
     "fine_int4": MoEShape("fine_int4", T=256, d=6144, E=256, k=8, f=2048, wdt="i4g128"),
     "skewed": MoEShape("skewed", T=16384, d=2048, E=64, k=4, f=1408, bias="zipf"),
+    # beside the five: the Mixtral-shaped prefill layer with int4 g128
+    # experts (~1024 rows per expert), for the int4 tensor-core GEMM
+    "mixtral_prefill_int4": MoEShape("mixtral_prefill_int4", T=4096, d=4096, E=8, k=2,
+                                     f=14336, wdt="i4g128"),
 }
 
 

@@ -27,6 +27,9 @@ SMALL = {
     "hot_expert": S("hot_expert", T=50, d=256, E=8, k=2, f=128, bias="hot0"),
     "one_token": S("one_token", T=1, d=256, E=8, k=2, f=128),
     "fp32_e64": S("fp32_e64", T=33, d=192, E=64, k=3, f=64, act="f32", wdt="f32"),
+    # int4 experts with hundreds of rows each: the tcgen05 grouped GEMM with
+    # the weights dequantised in shared memory
+    "int4_prefill": S("int4_prefill", T=600, d=512, E=4, k=2, f=384, wdt="i4g128"),
 }
 
 
@@ -46,14 +49,19 @@ def run_layer(s, lay, path=moe.PATH_AUTO):
     return layer, y, host_dict(dbg)
 
 
-def check_layer(s, lay, y, dbg, threads=1):
+def check_layer(s, lay, y, dbg, threads=1, sample=None):
     """Routing and dispatch of every token against the oracle, then the output
-    of every token that is not a near-tie, element by element."""
+    of every token that is not a near-tie (or of `sample` seeded tokens),
+    element by element."""
     idx, w, gap, inner = oracle_routing(s, lay)
     near = check_routing(dbg["topk_idx"], dbg["topk_w"], idx, w, gap, inner)
     check_dispatch(dbg, idx, near, s.E)
     assert np.allclose(dbg["gap"][~near], gap[~near], rtol=0, atol=1e-5)
     tokens = np.nonzero(~near)[0].astype(np.int32)
+    if sample is not None and sample < len(tokens):
+        pick = np.random.default_rng(0).choice(len(tokens), sample, replace=False)
+        tokens = np.sort(np.concatenate([tokens[pick], tokens[[0, -1]]]))
+        tokens = np.unique(tokens).astype(np.int32)
     ref = oracle.moe_forward(lay, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f, tokens=tokens,
                              threads=threads)
     got = y_to_f64(y)[tokens]
@@ -70,7 +78,7 @@ def test_forward_small(name):
     check_layer(s, lay, y, dbg)
 
 
-@pytest.mark.parametrize("name", ["decode_bf16", "prefill_bf16", "skew_small"])
+@pytest.mark.parametrize("name", ["decode_bf16", "prefill_bf16", "skew_small", "int4_prefill"])
 def test_paths_agree(name):
     """Decode (weight streaming) and prefill (tcgen05 grouped GEMM) paths give
     the same routing and outputs within rounding on the same inputs."""
@@ -115,6 +123,18 @@ def test_full_config(name):
     err, near = check_layer(s, lay, y, dbg, threads=os.cpu_count() or 1)
     print(f"{name}: path={layer.path_for(s.T)} rel_err={err:.3e} near_ties={near} "
           f"tokens_checked={s.T - near}")
+
+
+def test_full_int4_prefill_layer_sampled():
+    """The Mixtral-shaped layer with int4 experts at the prefill batch (the
+    bench's int4 tensor-core workload): routing and dispatch of every token,
+    outputs of 512 seeded tokens (every token would take the oracle ~10 min)."""
+    s = inputs.CONFIGS["mixtral_prefill_int4"]
+    lay = inputs.make_layer(s, seed=0)
+    layer, y, dbg = run_layer(s, lay)
+    assert layer.path_for(s.T) == moe.PATH_PREFILL
+    err, near = check_layer(s, lay, y, dbg, threads=os.cpu_count() or 1, sample=512)
+    print(f"mixtral_prefill_int4: rel_err={err:.3e} near_ties={near} tokens_checked=514")
 
 
 # ---------------------------------------------------------------- stages
@@ -248,6 +268,10 @@ EDGE = {
     "min_dims": S("min_dims", T=20, d=64, E=3, k=3, f=64),
     "e256_prefill": S("e256_prefill", T=2048, d=128, E=256, k=8, f=128),
     "int4_min": S("int4_min", T=12, d=128, E=5, k=2, f=128, wdt="i4g128"),
+    # int4 on the tensor cores: one scale group along d (K = 128), a down
+    # projection whose last 256-column tile is half past the weights, and an
+    # odd number of gate/up column tiles
+    "int4_tc_tails": S("int4_tc_tails", T=400, d=384, E=3, k=2, f=640, wdt="i4g128"),
 }
 
 
@@ -258,6 +282,18 @@ def test_edge_shapes(name, path):
     lay = inputs.make_layer(s, seed=41)
     _, y, dbg = run_layer(s, lay, path=path)
     check_layer(s, lay, y, dbg)
+
+
+def test_int4_prefill_many_tiles_per_cta():
+    """int4 experts on the tcgen05 path with several tiles per CTA (the
+    accumulator double buffer wraps, the converters cross tile boundaries):
+    every token against the oracle."""
+    s = S("int4_wrap", T=4096, d=1024, E=8, k=2, f=2048, wdt="i4g128")
+    lay = inputs.make_layer(s, seed=43)
+    layer, y, dbg = run_layer(s, lay)
+    assert layer.path_for(s.T) == moe.PATH_PREFILL
+    err, near = check_layer(s, lay, y, dbg, threads=os.cpu_count() or 1)
+    print(f"int4_wrap: rel_err={err:.3e} near_ties={near}")
 
 
 def test_empty_batch_is_a_no_op():
