@@ -122,7 +122,7 @@ struct coli_moe {
   int32_t* assign_row = nullptr;
   void* x_perm = nullptr;
   void* H = nullptr;
-  float* y_perm = nullptr;
+  void* y_perm = nullptr;  // fp32, or bf16 on the prefill forward
   float* y_part = nullptr;
   void* route_scratch = nullptr;
   void* perm_scratch = nullptr;
@@ -213,10 +213,13 @@ void harvest(coli_moe* h, TimingSet& ts) {
 // activations from x_tok[row_token[r]] and x_perm is not used. When the
 // decode path splits the down projection, partial slices go to h->y_part and
 // *splits_out > 1 (the caller sums them: the combine directly, the FFN stage
-// through a reduction).
-int run_ffn(coli_moe* h, const void* x_perm, const int32_t* offsets, int n_rows, float* y_perm,
+// through a reduction). With allow_bf16 the prefill path writes y_perm as
+// bf16 (half the bytes for the combine to read) and sets *y_bf16.
+int run_ffn(coli_moe* h, const void* x_perm, const int32_t* offsets, int n_rows, void* y_perm,
             int T, cudaStream_t st, TimingSet* ts, int* launches, int* splits_out, char* err,
-            size_t err_len, const void* x_tok = nullptr, const int32_t* row_token = nullptr) {
+            size_t err_len, const void* x_tok = nullptr, const int32_t* row_token = nullptr,
+            bool allow_bf16 = false, bool* y_bf16 = nullptr) {
+  if (y_bf16) *y_bf16 = false;
   const auto& c = h->cfg;
   const int E = c.n_experts, d = c.d_model, f = c.d_ff;
   int* status = device_status_ptr();
@@ -226,7 +229,8 @@ int run_ffn(coli_moe* h, const void* x_perm, const int32_t* offsets, int n_rows,
     CUDA_TRY(launch_f32_ffn(static_cast<const float*>(h->w.w_gu),
                             static_cast<const float*>(h->w.w_dn),
                             static_cast<const float*>(x_perm), offsets, n_rows, E, d, f,
-                            static_cast<float*>(h->H), y_perm, st, launches));
+                            static_cast<float*>(h->H), static_cast<float*>(y_perm), st,
+                            launches));
     timing_mark(h, ts, 3, st);
     timing_mark(h, ts, 4, st);
     return COLI_OK;
@@ -238,7 +242,8 @@ int run_ffn(coli_moe* h, const void* x_perm, const int32_t* offsets, int n_rows,
     CUDA_TRY(launch_tc_gateup(h->tc, x_perm, x_perm == h->x_perm, offsets, h->H, n_rows, st,
                               status));
     timing_mark(h, ts, 3, st);
-    CUDA_TRY(launch_tc_down(h->tc, h->H, offsets, y_perm, n_rows, st, status));
+    CUDA_TRY(launch_tc_down(h->tc, h->H, offsets, y_perm, allow_bf16, n_rows, st, status));
+    if (y_bf16) *y_bf16 = allow_bf16;
     timing_mark(h, ts, 4, st);
     *launches += 2;
     return COLI_OK;
@@ -270,7 +275,8 @@ int run_ffn(coli_moe* h, const void* x_perm, const int32_t* offsets, int n_rows,
                              i4 ? h->xsum : nullptr, h->dec_grid, st));
   } else {
     CUDA_TRY(launch_dec_down(h->w, static_cast<const __nv_bfloat16*>(h->H), offsets, E, d, f, 1,
-                             y_perm, 0, i4 ? h->xsum : nullptr, h->dec_grid, st));
+                             static_cast<float*>(y_perm), 0, i4 ? h->xsum : nullptr,
+                             h->dec_grid, st));
   }
   timing_mark(h, ts, 4, st);
   *launches += 2;
@@ -440,12 +446,19 @@ int coli_moe_forward(coli_moe* h, const void* x, int32_t T, void* y, void* strea
                           h->perm_scratch, st, status, &launches));
   timing_mark(h, ts, 2, st);
   int splits = 1;
+  bool y_bf16 = false;
   int rc = run_ffn(h, h->x_perm, h->offsets, n_rows, h->y_perm, T, st, ts, &launches, &splits,
-                   err, err_len, gather ? x : nullptr, gather ? h->row_token : nullptr);
+                   err, err_len, gather ? x : nullptr, gather ? h->row_token : nullptr,
+                   /*allow_bf16=*/c.act_dtype == COLI_BF16, &y_bf16);
   if (rc) return rc;
-  const float* part = splits > 1 ? h->y_part : h->y_perm;
-  CUDA_TRY(launch_combine(part, splits, static_cast<size_t>(n_rows) * d, h->assign_row,
-                          h->topk_w, T, k, d, c.act_dtype, y, st, status));
+  if (y_bf16) {
+    CUDA_TRY(launch_combine_bf16(static_cast<const __nv_bfloat16*>(h->y_perm), h->assign_row,
+                                 h->topk_w, T, k, d, c.act_dtype, y, st, status));
+  } else {
+    const float* part = splits > 1 ? h->y_part : static_cast<const float*>(h->y_perm);
+    CUDA_TRY(launch_combine(part, splits, static_cast<size_t>(n_rows) * d, h->assign_row,
+                            h->topk_w, T, k, d, c.act_dtype, y, st, status));
+  }
   launches += 1;
   timing_mark(h, ts, 5, st);
   if (ts) {

@@ -94,15 +94,21 @@ void tc_plan_destroy(TcPlan* plan);
 cudaError_t launch_tc_gateup(TcPlan* plan, const void* x_perm, bool own_x_perm,
                              const int32_t* offsets, void* H, int n_rows, cudaStream_t st,
                              int* status);
-// y_perm[rows][d] = H Wd^T per expert group (f32); H is the plan's buffer.
-cudaError_t launch_tc_down(TcPlan* plan, const void* H, const int32_t* offsets, float* y_perm,
-                           int n_rows, cudaStream_t st, int* status);
+// y_perm[rows][d] = H Wd^T per expert group, fp32 or (bf16_out) bf16 rounded
+// to nearest even; H is the plan's buffer.
+cudaError_t launch_tc_down(TcPlan* plan, const void* H, const int32_t* offsets, void* y_perm,
+                           bool bf16_out, int n_rows, cudaStream_t st, int* status);
 
 // ---- combine (A4) and helpers ----------------------------------------------------
 // Rows outside [0, T*k) are skipped and latch COLI_EDEVICE in *status.
 cudaError_t launch_combine(const float* y_part, int splits, size_t part_stride,
                            const int32_t* assign_row, const float* topk_w, int T, int k, int d,
                            int out_dt, void* y, cudaStream_t st, int* status);
+// Same merge from bf16 rows y_perm [T*k][d] (the prefill forward's output of
+// the down projection).
+cudaError_t launch_combine_bf16(const __nv_bfloat16* y_perm, const int32_t* assign_row,
+                                const float* topk_w, int T, int k, int d, int out_dt, void* y,
+                                cudaStream_t st, int* status);
 cudaError_t launch_reduce_splits(const float* y_part, int splits, size_t part_stride,
                                  int n_rows, int d, float* y_perm, cudaStream_t st);
 cudaError_t launch_repack(const void* src_gate, const void* src_up, const void* src_down,

@@ -139,7 +139,8 @@ COLI_DEV void convert_rows(uint32_t raw, uint32_t b, int ct, const uint32_t (&s2
   }
 }
 
-// EPI 0: gate/up + SwiGLU -> bf16 H [rows][N/2]; EPI 1: fp32 out [rows][N].
+// EPI 0: gate/up + SwiGLU -> bf16 H [rows][N/2]; EPI 1: fp32 out [rows][N];
+// EPI 2: bf16 out [rows][N].
 // I4: map_b is the int4 weight tensor (bytes [rows][K/2], box 256 x 32) and
 // the B operand is dequantised in shared memory by the converter warps.
 template <int EPI, bool I4>
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(Shape<I4>::kThreads, 1)
                                   packed[4 * v + 3]);
           }
         }
-      } else {
+      } else if constexpr (EPI == 1) {
         float* Y = static_cast<float*>(out);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -330,6 +331,24 @@ __global__ void __launch_bounds__(Shape<I4>::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        }
+      } else {  // EPI 2: bf16 out (round to nearest even)
+        __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(out);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c * 32, v);
+          const int col = tl.nt * BN + c * 32;
+          if (valid && col < N) {
+            uint32_t p[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              p[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            uint4* dst = reinterpret_cast<uint4*>(Y + static_cast<size_t>(row) * N + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
           }
         }
       }
@@ -477,11 +496,13 @@ cudaError_t tc_plan_create(TcPlan** plan, int wdt, const void* w_gu, const void*
     if (e == cudaSuccess) e = make_i4_map(&p->map_wdn, w_dn, static_cast<uint64_t>(E) * d, f);
     if (e == cudaSuccess) e = set_smem<0, true>();
     if (e == cudaSuccess) e = set_smem<1, true>();
+    if (e == cudaSuccess) e = set_smem<2, true>();
   } else {
     e = make_map(&p->map_wgu, w_gu, static_cast<uint64_t>(E) * 2 * f, d, BN);
     if (e == cudaSuccess) e = make_map(&p->map_wdn, w_dn, static_cast<uint64_t>(E) * d, f, BN);
     if (e == cudaSuccess) e = set_smem<0, false>();
     if (e == cudaSuccess) e = set_smem<1, false>();
+    if (e == cudaSuccess) e = set_smem<2, false>();
   }
   if (e == cudaSuccess) e = make_map(&p->map_xperm, x_perm, static_cast<uint64_t>(max_rows), d, BM);
   if (e == cudaSuccess) e = make_map(&p->map_h, H, static_cast<uint64_t>(max_rows), f, BM);
@@ -523,12 +544,15 @@ cudaError_t launch_tc_gateup(TcPlan* p, const void* x_perm, bool own_x_perm,
   return cudaGetLastError();
 }
 
-cudaError_t launch_tc_down(TcPlan* p, const void* H, const int32_t* offsets, float* y_perm,
-                           int n_rows, cudaStream_t st, int* status) {
+cudaError_t launch_tc_down(TcPlan* p, const void* H, const int32_t* offsets, void* y_perm,
+                           bool bf16_out, int n_rows, cudaStream_t st, int* status) {
   (void)H;  // always the plan's H buffer, mapped at create
   if (n_rows == 0) return cudaSuccess;
   const I4Args q4{p->s_dn, p->f / 128, p->E * p->d};
-  launch<1>(p, p->map_h, p->map_wdn, offsets, p->f, p->d, y_perm, q4, st, status);
+  if (bf16_out)
+    launch<2>(p, p->map_h, p->map_wdn, offsets, p->f, p->d, y_perm, q4, st, status);
+  else
+    launch<1>(p, p->map_h, p->map_wdn, offsets, p->f, p->d, y_perm, q4, st, status);
   return cudaGetLastError();
 }
 

@@ -57,6 +57,59 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The same merge from bf16 rows: a thread takes 8 consecutive columns of one
+// token (16 bytes of each of its k rows, all loads issued before the sums),
+// so a 256-thread block covers 2048 columns. Sums in fp32, j ascending.
+template <bool BF16_OUT>
+__global__ void __launch_bounds__(256)
+    k_combine_bf16(const uint4* __restrict__ y_perm, const int32_t* __restrict__ assign_row,
+                   const float* __restrict__ topk_w, int T, int k, int d, int n_rows,
+                   void* __restrict__ y, int* status) {
+  const int d8 = d / 8;
+  const long gid = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x;
+  if (gid >= static_cast<long>(T) * d8) return;
+  const int t = static_cast<int>(gid / d8), c = static_cast<int>(gid % d8);
+  constexpr int KMAX = 8;
+  uint4 v[KMAX];
+  float g[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    v[j] = make_uint4(0u, 0u, 0u, 0u);
+    g[j] = 0.f;
+    if (j < k) {
+      const size_t a = static_cast<size_t>(t) * k + j;
+      const int row = assign_row[a];
+      if (row >= 0 && row < n_rows) {
+        g[j] = topk_w[a];
+        v[j] = y_perm[static_cast<size_t>(row) * d8 + c];
+      } else {
+        latch_error(status, kErrDevice);
+      }
+    }
+  }
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    if (j < k) {
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(g[j], bf16_lo(w[i]), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(g[j], bf16_hi(w[i]), acc[2 * i + 1]);
+      }
+    }
+  }
+  if (BF16_OUT) {
+    reinterpret_cast<uint4*>(y)[gid] =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                   pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+  } else {
+    float4* dst = reinterpret_cast<float4*>(y) + 2 * gid;
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
 __global__ void __launch_bounds__(256)
     k_reduce_splits(const float* __restrict__ part, int splits, size_t part_stride, size_t n4,
                     float* __restrict__ out) {
@@ -257,6 +310,22 @@ cudaError_t launch_combine(const float* y_part, int splits, size_t part_stride,
   else
     k_combine<false><<<grid, threads, 0, st>>>(y_part, splits, part_stride, assign_row, topk_w,
                                                T, k, d, n_rows, y, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bf16(const __nv_bfloat16* y_perm, const int32_t* assign_row,
+                                const float* topk_w, int T, int k, int d, int out_dt, void* y,
+                                cudaStream_t st, int* status) {
+  if (T == 0) return cudaSuccess;
+  const long n = static_cast<long>(T) * (d / 8);
+  const unsigned grid = static_cast<unsigned>((n + 255) / 256);
+  const int n_rows = T * k;
+  if (out_dt == DT_BF16)
+    k_combine_bf16<true><<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(y_perm),
+                                               assign_row, topk_w, T, k, d, n_rows, y, status);
+  else
+    k_combine_bf16<false><<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(y_perm),
+                                                assign_row, topk_w, T, k, d, n_rows, y, status);
   return cudaGetLastError();
 }
 

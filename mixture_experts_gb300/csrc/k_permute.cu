@@ -189,12 +189,19 @@ __global__ void __launch_bounds__(kThreads)
   scatter_range(topk_idx, a0, a1, E, k, base, wcnt, tot, row_token, assign_row);
 }
 
-// x_perm[r] = x[row_token[r]], one warp per row, 16-byte vectors.
+// x_perm[r] = x[row_token[r]], one warp per row, 16-byte vectors. Each token
+// row is read k times, far apart in time (rows are in expert order), while
+// the T*k-row copy streams through L2: the reads carry an L2 evict-last
+// policy and the writes evict-first, so x stays in L2 and is read from DRAM
+// about once.
 __global__ void __launch_bounds__(256)
     k_gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ row_token, int n_rows,
                   int T, int vec_per_row, uint4* __restrict__ x_perm, int* status) {
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * 8;
+  uint64_t keep, stream;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream));
   for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < n_rows; r += warps) {
     const int t = row_token[r];
     if (t < 0 || t >= T) {
@@ -203,7 +210,15 @@ __global__ void __launch_bounds__(256)
     }
     const uint4* src = x + static_cast<size_t>(t) * vec_per_row;
     uint4* dst = x_perm + static_cast<size_t>(r) * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) dst[v] = src[v];
+    for (int v = lane; v < vec_per_row; v += 32) {
+      uint4 u;
+      asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                   : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                   : "l"(src + v), "l"(keep));
+      asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(dst + v),
+                   "r"(u.x), "r"(u.y), "r"(u.z), "r"(u.w), "l"(stream)
+                   : "memory");
+    }
   }
 }
 

@@ -30,6 +30,8 @@ namespace coli {
 namespace {
 
 constexpr int kWarps = 8;
+// bf16 batches of at least this many tokens take the one-launch tiled router
+constexpr int kTiledMinTokens = 1024;
 
 COLI_DEV void load8(const float* p, float (&v)[8]) {
   const float4 a = *reinterpret_cast<const float4*>(p);
@@ -259,6 +261,88 @@ __global__ void __launch_bounds__(128)
     }
 }
 
+// Order-preserving integer key of a float: a larger float gets a larger key
+// (-0 is folded into +0 first, so the two compare equal as floats do). Key 0
+// is below every float, including -inf.
+COLI_DEV uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v + 0.f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+COLI_DEV float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// One warp, one token: lane holds the logits of experts lane + 32 i (-inf
+// past E). k+1 rounds of warp arg-max (larger value, then lower index) give
+// the top-k in descending order and the k-th/(k+1)-th gap. A round is one
+// warp max over the order keys and one warp min over the indices of the
+// lanes that hold that key. The gates are exp(l_j - l_max) / sum_j'
+// exp(l_j' - l_max), summed with j ascending.
+template <int PER_LANE>
+COLI_DEV void select_token(const float (&l)[PER_LANE], int E, int k, int t,
+                           int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                           float* __restrict__ gap) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[PER_LANE];
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) key[i] = (lane + 32 * i < E) ? order_key(l[i]) : 0u;
+  float sel_val[8];
+  int sel_idx[8];
+  float kth = 0.f, next = INFINITY;  // l_(k) and l_(k+1)
+  const int rounds = min(k + 1, E);
+#pragma unroll
+  for (int r = 0; r < 9; ++r) {
+    if (r < 8) {
+      sel_val[r] = -INFINITY;
+      sel_idx[r] = 0;
+    }
+    if (r < rounds) {
+      // this lane's best remaining key (lower slot = lower index on ties)
+      uint32_t best = 0u;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < PER_LANE; ++i)
+        if (key[i] > best) {
+          best = key[i];
+          bi = lane + 32 * i;
+        }
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, best);
+      const uint32_t cand = (best == kmax && best != 0u) ? static_cast<uint32_t>(bi) : 0xffffffffu;
+      const int win = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
+      if ((win & 31) == lane) {
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i)
+          if (i == (win >> 5)) key[i] = 0u;  // taken
+      }
+      const float v = key_value(kmax);
+      if (r < 8) {
+        sel_val[r] = v;
+        sel_idx[r] = win;
+      }
+      if (r == k - 1) kth = v;
+      if (r == k) next = v;
+    }
+  }
+  if (gap != nullptr && lane == 0) gap[t] = (k < E) ? kth - next : INFINITY;
+  const float best0 = sel_val[0];
+  float den = 0.f, mine = 0.f;
+  int id = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j < k) {
+      const float ex = expf(sel_val[j] - best0);
+      den += ex;
+      if (j == lane) {
+        mine = ex;
+        id = sel_idx[j];
+      }
+    }
+  if (lane < k) {
+    topk_idx[static_cast<size_t>(t) * k + lane] = id;
+    topk_w[static_cast<size_t>(t) * k + lane] = mine / den;
+  }
+}
+
 template <int PER_LANE>
 __global__ void __launch_bounds__(kWarps * 32)
     k_route_select(const float* __restrict__ part, int slices, const float* __restrict__ b,
@@ -280,54 +364,298 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
     l[i] = v;
   }
-  unsigned taken = 0;  // bit i: slot i of this lane already selected
-  float best0 = 0.f, prev = 0.f, den = 0.f;
-  float sel_val[8];
-  int sel_idx[8];
-  const int rounds = min(k + 1, E);
-  for (int r = 0; r < rounds; ++r) {
-    float bv = -INFINITY;
-    int bi = 1 << 30;
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !(taken & (1u << i)) && beats(l[i], e, bv, bi)) {
-        bv = l[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (beats(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (r < k) {
-      sel_val[r] = bv;
-      sel_idx[r] = bi;
-    }
-    if (r == 0) best0 = bv;
-    if (r == k - 1) prev = bv;
-    if (r == k && gap != nullptr && lane == 0) gap[t] = prev - bv;
+  select_token<PER_LANE>(l, E, k, t, topk_idx, topk_w, gap);
+}
+
+// ---- bf16, many tokens: one launch ------------------------------------------------
+// A block takes 32 tokens and all E experts. Its 8 warps compute the logits
+// with mma.sync m16n8k16 (tokens M, experts N, both m-tiles of the block per
+// warp so each W_r fragment feeds two MMAs): with NT = ceil(E/8) expert
+// tiles, warp w takes expert tiles w % G, w % G + G, ... (G = 8 / ks groups)
+// over the ks-th part w / G of the reduction (ks = 8 / NT splits when NT < 8,
+// so small E still keeps all warps busy). Every 32-index step goes into a
+// zeroed accumulator that is then added with an FADD (fp32 sum of 32-term
+// partials, as in the two-launch path), four steps in flight on four running
+// sums. Partial logits meet in shared memory, summed over the reduction
+// parts in fixed order, plus the bias; then each warp selects for 4 tokens.
+constexpr int kTok = 32;
+
+__global__ void __launch_bounds__(256)
+    k_route_tc(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,
+               const float* __restrict__ b, int T, int d, int E, int k, int ks,
+               int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+               float* __restrict__ gap, int* status) {
+  extern __shared__ float sl[];  // [ks][kTok][E] partial logits
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const int t0 = blockIdx.x * kTok;
+  const int NT = (E + 7) / 8;
+  const int G = 8 / ks;
+  const int grp = warp % G, kp = warp / G;
+  const int steps = d / 32;
+  const int s0 = steps * kp / ks, s1 = steps * (kp + 1) / ks;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  // The block's token rows are its only DRAM stream and its warps walk them
+  // together a few steps ahead: bring them all into L2 at once (one bulk
+  // prefetch per row) so the loads below wait on L2, not on DRAM.
+  if (threadIdx.x < kTok && t0 + threadIdx.x < T) {
+    const __nv_bfloat16* row = x + static_cast<size_t>(t0 + threadIdx.x) * d;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row),
+                 "r"(static_cast<uint32_t>(d * 2))
+                 : "memory");
   }
-  if (k == E && gap != nullptr && lane == 0) gap[t] = INFINITY;
-  // gates: exp(l_j - l_max) / sum_j' exp(l_j' - l_max), j ascending
-  for (int j = 0; j < k; ++j) den += expf(sel_val[j] - best0);
-  if (lane < k) {
+  const __nv_bfloat16* xr[2][2];
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = t0 + 16 * m + g + 8 * h;
+      xr[m][h] = t < T ? x + static_cast<size_t>(t) * d + q * 8 : nullptr;
+    }
+  for (int nt = grp; nt < NT; nt += G) {
+    const int e = nt * 8 + g;
+    const __nv_bfloat16* wr = e < E ? w + static_cast<size_t>(e) * d + q * 8 : nullptr;
+    constexpr int U = 4;
+    float acc[U][2][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[u][m][c] = 0.f;
+    for (int s = s0; s < s1; s += U) {
+      uint4 a[U][2][2], bw[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const bool in = s + u < s1;
+        const int kk = (s + u) * 32;
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            a[u][m][h] = (in && xr[m][h]) ? *reinterpret_cast<const uint4*>(xr[m][h] + kk) : z;
+        bw[u] = (in && wr) ? *reinterpret_cast<const uint4*>(wr + kk) : z;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          float t4[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_bf16_16816(t4, a[u][m][0].x, a[u][m][1].x, a[u][m][0].y, a[u][m][1].y, bw[u].x,
+                         bw[u].y);
+          mma_bf16_16816(t4, a[u][m][0].z, a[u][m][1].z, a[u][m][0].w, a[u][m][1].w, bw[u].z,
+                         bw[u].w);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[u][m][c] += t4[c];
+        }
+    }
+    // (sum0 + sum1) + (sum2 + sum3), then the block's shared partial table
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float v = (acc[0][m][c] + acc[1][m][c]) + (acc[2][m][c] + acc[3][m][c]);
+        const int tl = 16 * m + g + ((c & 2) ? 8 : 0);
+        const int ee = nt * 8 + 2 * q + (c & 1);
+        if (ee < E) sl[(static_cast<size_t>(kp) * kTok + tl) * E + ee] = v;
+      }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kTok * E; i += blockDim.x) {
     float v = 0.f;
-    int id = 0;
-    for (int j = 0; j < k; ++j)
-      if (j == lane) {
-        v = sel_val[j];
-        id = sel_idx[j];
-      }
-    topk_idx[static_cast<size_t>(t) * k + lane] = id;
-    topk_w[static_cast<size_t>(t) * k + lane] = expf(v - best0) / den;
+    for (int p = 0; p < ks; ++p) v += sl[static_cast<size_t>(p) * kTok * E + i];
+    if (b != nullptr) v += b[i % E];
+    sl[i] = v;
   }
+  __syncthreads();
+#define COLI_SELECT_TOKENS(PL)                                                    \
+  for (int j = 0; j < kTok / 8; ++j) {                                            \
+    const int tl = warp * (kTok / 8) + j, t = t0 + tl;                            \
+    if (t >= T) break;                                                            \
+    float l[PL];                                                                  \
+    _Pragma("unroll") for (int i = 0; i < PL; ++i) {                              \
+      const int e = lane + 32 * i;                                                \
+      l[i] = e < E ? rankable(sl[tl * E + e], status) : -INFINITY;               \
+    }                                                                             \
+    select_token<PL>(l, E, k, t, topk_idx, topk_w, gap);                          \
+  }
+  if (E <= 32) {
+    COLI_SELECT_TOKENS(1)
+  } else if (E <= 64) {
+    COLI_SELECT_TOKENS(2)
+  } else if (E <= 128) {
+    COLI_SELECT_TOKENS(4)
+  } else {
+    COLI_SELECT_TOKENS(8)
+  }
+#undef COLI_SELECT_TOKENS
+}
+
+// ---- bf16, many tokens, E > 32: one launch, pipelined -------------------------------
+// A block takes 64 tokens and all E experts. The reduction runs in chunks of
+// KC indices: 256 threads copy the chunk's token rows and W_r rows into a
+// 3-stage shared-memory ring with 16-byte cp.async (rows past T or E are
+// zero-filled), row pitch KC*2 + 64 bytes so the fragment loads of a
+// quarter-warp hit 8 distinct bank groups. Warp w owns expert tiles w, w+8,
+// w+16, w+24 (8 experts each) for all four 16-token tiles; each 64 indices
+// go into a fresh mma.sync accumulator (zero input) that is added to the
+// running sum with an FADD, so the tensor core never carries a sum across
+// more than 64 products. The ring is then reused for the [64][E]
+// logit table, plus the bias, and each warp selects for 8 tokens.
+constexpr int kBigTok = 64;
+constexpr int kBigStages = 3;
+
+COLI_DEV void cp_async16_zfill(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+template <int KC>
+constexpr int big_pitch() { return KC * 2 + 64; }
+
+template <int KC>
+size_t big_smem_bytes(int E) {
+  const size_t ring = static_cast<size_t>(kBigStages) * (kBigTok + ((E + 7) / 8) * 8) *
+                      big_pitch<KC>();
+  const size_t table = static_cast<size_t>(kBigTok) * E * sizeof(float);
+  return ring > table ? ring : table;
+}
+
+template <int KC>
+__global__ void __launch_bounds__(256, 1)
+    k_route_tc_big(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,
+                   const float* __restrict__ b, int T, int d, int E, int k,
+                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                   float* __restrict__ gap, int* status) {
+  extern __shared__ __align__(16) uint8_t rsm[];
+  constexpr int P = big_pitch<KC>();
+  constexpr int CH = KC / 8;  // 16-byte pieces per row and chunk
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const int t0 = blockIdx.x * kBigTok;
+  const int NT = (E + 7) / 8, Ep = NT * 8;
+  const int rows = kBigTok + Ep;  // token rows, then expert rows, per stage
+  const uint32_t base = smem_u32(rsm);
+  const uint32_t stage_bytes = static_cast<uint32_t>(rows) * P;
+  const int chunks = d / KC;
+
+  // this thread's copies of a chunk: fixed (row, piece) pairs, so the source
+  // pointers and shared offsets are computed once; a chunk moves them by KC
+  constexpr int kMaxPieces = (kBigTok + (KC == 128 ? 128 : 256)) * CH / 256;
+  const __nv_bfloat16* src0[kMaxPieces];
+  uint32_t dst0[kMaxPieces];
+  uint32_t valid_mask = 0, live_mask = 0;
+#pragma unroll
+  for (int u = 0; u < kMaxPieces; ++u) {
+    const int i = threadIdx.x + 256 * u;
+    const int r = i / CH, piece = i % CH;
+    const bool live = r < rows;
+    const bool tok = r < kBigTok;
+    const int src_row = tok ? t0 + r : r - kBigTok;
+    const bool valid = live && (tok ? src_row < T : src_row < E);
+    src0[u] = (tok ? x : w) + (valid ? static_cast<size_t>(src_row) * d : 0) + piece * 8;
+    dst0[u] = r * P + piece * 16;
+    if (valid) valid_mask |= 1u << u;
+    if (live) live_mask |= 1u << u;
+  }
+  auto issue = [&](int c) {
+    if (c < chunks) {
+      const uint32_t sb = base + (c % kBigStages) * stage_bytes;
+#pragma unroll
+      for (int u = 0; u < kMaxPieces; ++u)
+        if (live_mask & (1u << u))
+          cp_async16_zfill(sb + dst0[u], src0[u] + c * KC, (valid_mask >> u) & 1u);
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int c = 0; c < kBigStages - 1; ++c) issue(c);
+
+  float acc[4][4][4];  // [expert tile slot][token tile][c]
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[j][m][c] = 0.f;
+
+  for (int c = 0; c < chunks; ++c) {
+    cp_async_wait<kBigStages - 2>();  // chunk c has landed (this thread's copies)
+    __syncthreads();                  // ... and everyone's; the slot of chunk c-1 is free
+    issue(c + kBigStages - 1);
+    const uint32_t sb = base + (c % kBigStages) * stage_bytes;
+    // 64 indices (two 32-index steps, four MMAs) per fresh accumulator
+#pragma unroll
+    for (int st = 0; st < KC / 32; st += 2) {
+      uint4 a[2][4][2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            a[u][m][h] = lds128(sb + (16 * m + g + 8 * h) * P + (st + u) * 64 + q * 16);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int nt = warp + 8 * j;
+        if (nt < NT) {
+          uint4 bw[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            bw[u] = lds128(sb + (kBigTok + nt * 8 + g) * P + (st + u) * 64 + q * 16);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            float t4[4];
+            mma_bf16_16816_z(t4, a[0][m][0].x, a[0][m][1].x, a[0][m][0].y, a[0][m][1].y,
+                             bw[0].x, bw[0].y);
+            mma_bf16_16816(t4, a[0][m][0].z, a[0][m][1].z, a[0][m][0].w, a[0][m][1].w, bw[0].z,
+                           bw[0].w);
+            mma_bf16_16816(t4, a[1][m][0].x, a[1][m][1].x, a[1][m][0].y, a[1][m][1].y, bw[1].x,
+                           bw[1].y);
+            mma_bf16_16816(t4, a[1][m][0].z, a[1][m][1].z, a[1][m][0].w, a[1][m][1].w, bw[1].z,
+                           bw[1].w);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) acc[j][m][cc] += t4[cc];
+          }
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();  // the ring becomes the logit table
+  float* lt = reinterpret_cast<float*>(rsm);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int nt = warp + 8 * j;
+    if (nt >= NT) continue;
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int tl = 16 * m + g + ((cc & 2) ? 8 : 0);
+        const int e = nt * 8 + 2 * q + (cc & 1);
+        if (e < E) lt[tl * E + e] = acc[j][m][cc] + (b != nullptr ? b[e] : 0.f);
+      }
+  }
+  __syncthreads();
+#define COLI_SELECT_BIG(PL)                                                       \
+  for (int jt = 0; jt < kBigTok / 8; ++jt) {                                      \
+    const int tl = warp * (kBigTok / 8) + jt, t = t0 + tl;                        \
+    if (t >= T) break;                                                            \
+    float l[PL];                                                                  \
+    _Pragma("unroll") for (int i = 0; i < PL; ++i) {                              \
+      const int e = lane + 32 * i;                                                \
+      l[i] = e < E ? rankable(lt[tl * E + e], status) : -INFINITY;               \
+    }                                                                             \
+    select_token<PL>(l, E, k, t, topk_idx, topk_w, gap);                          \
+  }
+  if (E <= 64) {
+    COLI_SELECT_BIG(2)
+  } else if (E <= 128) {
+    COLI_SELECT_BIG(4)
+  } else {
+    COLI_SELECT_BIG(8)
+  }
+#undef COLI_SELECT_BIG
 }
 
 int slices_for(int d) { return (d + kKS - 1) / kKS; }
@@ -336,6 +664,8 @@ int slices_for(int d) { return (d + kKS - 1) / kKS; }
 
 size_t route_scratch_bytes(int T, int d, int E) {
   if (E <= 32 || T <= 0) return 0;
+  // (bf16 batches of kTiledMinTokens or more need none; the size does not
+  // depend on the dtype, so callers may always pass this much)
   const size_t n = static_cast<size_t>(slices_for(d)) * T * E * sizeof(float);
   return (n + 255) & ~static_cast<size_t>(255);
 }
@@ -346,6 +676,50 @@ cudaError_t launch_route(const void* x, const void* w_r, const float* b_r, int T
   if (T == 0) return cudaSuccess;
   const dim3 block(kWarps * 32);
   const dim3 grid((T + kWarps - 1) / kWarps);
+  if (act == DT_BF16 && T >= kTiledMinTokens && E > 32) {
+    // many tokens, many experts: one launch, 64 tokens per block, pipelined
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static bool attr_set[2][128] = {};  // per kernel and device: more than 48 KiB of smem
+    if (d % 128 == 0 && E <= 128) {
+      const size_t smem = big_smem_bytes<128>(E);
+      if (dev >= 0 && dev < 128 && !attr_set[0][dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            k_route_tc_big<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            static_cast<int>(big_smem_bytes<128>(128)));
+        if (e != cudaSuccess) return e;
+        attr_set[0][dev] = true;
+      }
+      k_route_tc_big<128><<<(T + kBigTok - 1) / kBigTok, 256, smem, st>>>(
+          static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_r), b_r, T,
+          d, E, k, topk_idx, topk_w, gap, status);
+    } else {
+      const size_t smem = big_smem_bytes<64>(E);
+      if (dev >= 0 && dev < 128 && !attr_set[1][dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            k_route_tc_big<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            static_cast<int>(big_smem_bytes<64>(256)));
+        if (e != cudaSuccess) return e;
+        attr_set[1][dev] = true;
+      }
+      k_route_tc_big<64><<<(T + kBigTok - 1) / kBigTok, 256, smem, st>>>(
+          static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_r), b_r, T,
+          d, E, k, topk_idx, topk_w, gap, status);
+    }
+    if (n_launches) *n_launches += 1;
+    return cudaGetLastError();
+  }
+  if (act == DT_BF16 && T >= kTiledMinTokens) {
+    // many tokens, E <= 32: one launch, 32 tokens per block, logits on the tensor cores
+    const int NT = (E + 7) / 8;
+    const int ks = NT >= 8 ? 1 : 8 / NT;
+    const size_t smem = static_cast<size_t>(ks) * kTok * E * sizeof(float);
+    k_route_tc<<<(T + kTok - 1) / kTok, 256, smem, st>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_r), b_r, T, d,
+        E, k, ks, topk_idx, topk_w, gap, status);
+    if (n_launches) *n_launches += 1;
+    return cudaGetLastError();
+  }
   if (E <= 32) {
 #define COLI_ROUTE_FUSED(TA, EM)                                                             \
   k_route_fused<TA, EM><<<T, block, 0, st>>>(static_cast<const TA*>(x),                 \

@@ -168,6 +168,32 @@ def test_stage_route_topk(E, k, act, bias):
     assert np.max(np.abs(g[fin] - r_gap[fin]), initial=0.0) <= 3e-6
 
 
+@pytest.mark.parametrize("E,k,bias", [(3, 1, False), (8, 2, True), (24, 3, False), (40, 5, True),
+                                      (64, 4, True), (200, 7, False), (256, 8, False)])
+def test_stage_route_topk_many_tokens(E, k, bias):
+    """bf16 batches of 1024+ tokens take the one-launch router (32 tokens per
+    block, tensor-core logits, the reduction split over warps when E is small):
+    expert counts that fill one, some or all of the block's warps, a ragged
+    last block, with and without bias."""
+    T, d = 1100, 384
+    s = S("route_many", T=T, d=d, E=E, k=k, f=64, bias="zipf" if bias else "none")
+    lay, dev = _stage_layer(s, 22)
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    gap = torch.empty(T, dtype=torch.float32, device="cuda")
+    nb = moe.coli_route_scratch_bytes(T, d, E)
+    scratch = torch.empty(max(nb, 1), dtype=torch.uint8, device="cuda")
+    rc = moe.coli_route_topk(dev["x"], dev["w_router"], dev["b_router"], T, d, E, k, s.act_code,
+                             idx, w, gap, scratch, nb)
+    assert rc == 0, moe.last_error()
+    r_idx, r_w, r_gap, r_inner = oracle_routing(s, lay)
+    near = check_routing(idx.cpu().numpy(), w.cpu().numpy(), r_idx, r_w, r_gap, r_inner)
+    g = gap.cpu().numpy()
+    fin = ~near & np.isfinite(r_gap)
+    assert np.max(np.abs(g[fin] - r_gap[fin]), initial=0.0) <= 3e-6
+    assert moe.coli_device_status() == moe.COLI_OK
+
+
 @pytest.mark.parametrize("T,E,k,act", [(37, 8, 2, "bf16"), (300, 64, 4, "f32"),
                                        (5000, 64, 4, "bf16"), (3000, 256, 8, "bf16"),
                                        (1, 1, 1, "bf16")])
