@@ -20,6 +20,13 @@ Recipe (fixed so every run of every consumer sees the same bits):
   s = bf16(max|w| / 7) and q = clamp(round_half_even(w / s), -7, 7) (q = 0 when
   s = 0), packed two's-complement, low nibble = even index; scales bf16
   [..][cols/128].
+* MX experts (OCP Microscaling): per output row and per 32 consecutive
+  reduction indices, the shared exponent is floor(log2(max|w|)) - emax with
+  emax = 8 (E4M3) or 2 (E2M1); the scale byte is that exponent + 127 (E8M0;
+  127 for an all-zero block); each element is w / 2^exponent rounded to
+  nearest even in the element format and saturated at its largest normal
+  (448, 6). E4M3 codes are bytes [..][cols]; E2M1 codes are nibbles packed
+  two per byte, low nibble = even index; scales [..][cols/32].
 * Router bias: none, or the skewed-routing rule
   b_e = alpha * ln p(rank(e)) with Zipf(s) popularity p(r) = r^-s / H over the
   ranks r = 1..E, the ranks assigned by a seeded permutation; alpha is the
@@ -36,9 +43,11 @@ from dataclasses import dataclass, replace
 
 import torch
 
-F32, BF16, I4G128 = 0, 1, 2
-DTYPE_CODE = {"f32": F32, "bf16": BF16, "i4g128": I4G128}
+F32, BF16, I4G128, MXFP8, MXFP4 = 0, 1, 2, 3, 4
+DTYPE_CODE = {"f32": F32, "bf16": BF16, "i4g128": I4G128, "mxfp8": MXFP8, "mxfp4": MXFP4}
 GROUP = 128
+MX_BLOCK = 32
+E2M1_GRID = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)  # magnitudes of codes 0..7
 
 # Zipf exponent and the bias scale chosen for the skewed-routing layer
 # (T=16384, d=2048, E=64, k=4, seed 0).
@@ -55,7 +64,7 @@ class MoEShape:
     k: int
     f: int
     act: str = "bf16"      # "f32" | "bf16"
-    wdt: str = "bf16"      # "f32" | "bf16" | "i4g128"
+    wdt: str = "bf16"      # "f32" | "bf16" | "i4g128" | "mxfp8" | "mxfp4"
     bias: str = "none"     # "none" | "zipf" | "hot0"
     alpha: float = SKEWED_ALPHA
 
@@ -109,6 +118,35 @@ def quantize_i4g128(w: torch.Tensor):
     nib = (q & 0xF).to(torch.uint8)
     packed = nib[:, 0::2] | (nib[:, 1::2] << 4)
     return packed.contiguous(), s.contiguous()
+
+
+def quantize_mx(w: torch.Tensor, fmt: str):
+    """fp32 [rows][cols] -> (codes, E8M0 scales uint8 [rows][cols/32]) for
+    fmt "mxfp8" (E4M3 bytes [rows][cols]) or "mxfp4" (E2M1 nibbles packed
+    [rows][cols/2])."""
+    rows, cols = w.shape
+    assert cols % MX_BLOCK == 0, "MX blocks need cols % 32 == 0"
+    g = w.reshape(rows, cols // MX_BLOCK, MX_BLOCK)
+    amax = g.abs().amax(dim=-1)
+    emax = 8 if fmt == "mxfp8" else 2
+    _, ex = torch.frexp(amax)                      # amax = m * 2^ex, m in [0.5, 1)
+    shared = torch.where(amax > 0, ex.to(torch.int32) - 1 - emax, torch.zeros_like(ex))
+    shared = shared.clamp(-127, 127)
+    scales = (shared + 127).to(torch.uint8)
+    v = g / torch.pow(2.0, shared.to(torch.float32)).unsqueeze(-1)
+    if fmt == "mxfp8":
+        codes = v.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        return codes.reshape(rows, cols).contiguous(), scales.contiguous()
+    a = v.abs().clamp(max=6.0).double()
+    grid = torch.tensor(E2M1_GRID, dtype=torch.float64)
+    mids = (grid[1:] + grid[:-1]) / 2
+    code = torch.bucketize(a, mids, right=False)   # a == mids[j] -> j (lower neighbour)
+    tie = (code < 7) & (a == mids[code.clamp(max=6)]) & (code % 2 == 1)
+    code = code + tie.to(code.dtype)               # ties go to the even code
+    code = code.to(torch.uint8) | (torch.signbit(v).to(torch.uint8) << 3)
+    code = code.reshape(rows, cols)
+    packed = code[:, 0::2] | (code[:, 1::2] << 4)
+    return packed.contiguous(), scales.contiguous()
 
 
 def zipf_bias(E: int, alpha: float, perm: torch.Tensor, s: float = ZIPF_S) -> torch.Tensor:
@@ -171,6 +209,22 @@ def make_layer(shape: MoEShape, seed: int = 0, experts: bool = True) -> dict:
             wg[e], sg[e] = quantize_i4g128(torch.randn(f, d, generator=ge) * 0.02)
             wu[e], su[e] = quantize_i4g128(torch.randn(f, d, generator=ge) * 0.02)
             wd[e], sd[e] = quantize_i4g128(torch.randn(d, f, generator=ge) * 0.02)
+        _draw_experts(E, seed, one)
+        out.update(w_gate=wg, w_up=wu, w_down=wd, s_gate=sg, s_up=su, s_down=sd)
+    elif shape.wdt in ("mxfp8", "mxfp4"):
+        assert d % MX_BLOCK == 0 and f % MX_BLOCK == 0
+        bpe = 1 if shape.wdt == "mxfp8" else 2     # elements per byte
+        wg = torch.empty(E, f, d // bpe, dtype=torch.uint8)
+        wu = torch.empty(E, f, d // bpe, dtype=torch.uint8)
+        wd = torch.empty(E, d, f // bpe, dtype=torch.uint8)
+        sg = torch.empty(E, f, d // MX_BLOCK, dtype=torch.uint8)
+        su = torch.empty(E, f, d // MX_BLOCK, dtype=torch.uint8)
+        sd = torch.empty(E, d, f // MX_BLOCK, dtype=torch.uint8)
+
+        def one(e, ge):
+            wg[e], sg[e] = quantize_mx(torch.randn(f, d, generator=ge) * 0.02, shape.wdt)
+            wu[e], su[e] = quantize_mx(torch.randn(f, d, generator=ge) * 0.02, shape.wdt)
+            wd[e], sd[e] = quantize_mx(torch.randn(d, f, generator=ge) * 0.02, shape.wdt)
         _draw_experts(E, seed, one)
         out.update(w_gate=wg, w_up=wu, w_down=wd, s_gate=sg, s_up=su, s_down=sd)
     else:

@@ -10,7 +10,9 @@ with the CUDA library and never imports it.
 
 Arrays are numpy (or CPU torch tensors, converted here). bf16 data travels as
 its raw 16-bit patterns (``uint16``); int4 weights as packed bytes plus bf16
-scales. dtype codes: 0 = f32, 1 = bf16, 2 = int4 with 128-wide groups.
+scales. dtype codes: 0 = f32, 1 = bf16, 2 = int4 with 128-wide groups,
+3 = MXFP8 (E4M3 bytes), 4 = MXFP4 (E2M1 nibbles), both with E8M0 scale bytes
+per 32 reduction indices.
 """
 from __future__ import annotations
 
@@ -21,7 +23,7 @@ import threading
 
 import numpy as np
 
-F32, BF16, I4G128 = 0, 1, 2
+F32, BF16, I4G128, MXFP8, MXFP4 = 0, 1, 2, 3, 4
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.cpp")
 _LIB = os.path.join(_HERE, "libmoe_oracle.so")
@@ -60,6 +62,8 @@ def _lib():
             h.oracle_float_to_bf16.restype = ctypes.c_uint16
             h.oracle_weight_at.argtypes = [vp, vp, i, i, i, i, i, i]
             h.oracle_weight_at.restype = f64
+            h.oracle_mx_element.argtypes = [i, i]
+            h.oracle_mx_element.restype = f64
             h.oracle_router_logits.argtypes = [vp, i, vp, vp, i, i, i, _f32p]
             h.oracle_select_topk.argtypes = [_f32p, i, i, i, _i32p, _f32p, vp, vp]
             h.oracle_dispatch.argtypes = [_i32p, i, i, i, _i32p, _i32p, vp, vp]
@@ -113,6 +117,12 @@ def float_to_bf16(v: float) -> int:
 def weight_at(w, s, w_dt, e, rows, cols, r, c) -> float:
     w, s = to_np(w), to_np(s)
     return float(_lib().oracle_weight_at(_ptr(w), _ptr(s), w_dt, e, rows, cols, r, c))
+
+
+def mx_element(w_dt, code) -> float:
+    """Value of one E4M3 (w_dt MXFP8) or E2M1 (MXFP4) code, or of an E8M0
+    scale code (any other w_dt)."""
+    return float(_lib().oracle_mx_element(w_dt, int(code)))
 
 
 def router_logits(x, act_dt, w_r, b_r, T, d, E):

@@ -31,7 +31,9 @@
 // SwiGLU FFN has no biases, silu(z) = z / (1 + e^-z); within an expert group
 // rows keep token order (the counting sort is stable); int4 is a signed
 // two's-complement nibble (low nibble = even reduction index) times a bf16
-// scale shared by 128 consecutive reduction indices of one output row.
+// scale shared by 128 consecutive reduction indices of one output row; MX
+// weights are OCP E4M3 bytes or E2M1 nibbles (low nibble = even index) times
+// an E8M0 power of two shared by 32 consecutive reduction indices.
 //
 // Parity status: selection, gates, dispatch, the dense FFN special cases, the
 // int4 decode and the bf16 rounding are pinned by the CPU tests; end-to-end
@@ -48,8 +50,33 @@
 
 namespace {
 
-enum DType { DT_F32 = 0, DT_BF16 = 1, DT_I4G128 = 2 };
-constexpr int kGroup = 128;  // int4 scale group along the reduction index
+enum DType { DT_F32 = 0, DT_BF16 = 1, DT_I4G128 = 2, DT_MXFP8 = 3, DT_MXFP4 = 4 };
+constexpr int kGroup = 128;   // int4 scale group along the reduction index
+constexpr int kMxBlock = 32;  // MX scale block along the reduction index
+
+// OCP Microscaling (MX) element and scale formats, decoded exactly from their
+// definitions (the block-scaled weight formats of the model families in
+// [DD]'s table):
+//   E4M3: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is
+//         subnormal (2^-6 * m/8); S.1111.111 is NaN; no infinities.
+//   E2M1: sign, 2 exponent bits (bias 1), 1 mantissa bit; exponent 0 is
+//         subnormal (m/2); values 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+//   E8M0: the block scale 2^(s - 127); s = 255 is NaN.
+double e4m3_value(uint8_t b) {
+  const int sgn = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  if (e == 15 && m == 7) return std::numeric_limits<double>::quiet_NaN();
+  const double mag = e == 0 ? std::ldexp(m / 8.0, -6) : std::ldexp(1.0 + m / 8.0, e - 7);
+  return sgn ? -mag : mag;
+}
+double e2m1_value(uint8_t nib) {
+  const int sgn = (nib >> 3) & 1, e = (nib >> 1) & 3, m = nib & 1;
+  const double mag = e == 0 ? m / 2.0 : std::ldexp(1.0 + m / 2.0, e - 1);
+  return sgn ? -mag : mag;
+}
+double e8m0_value(uint8_t s) {
+  if (s == 255) return std::numeric_limits<double>::quiet_NaN();
+  return std::ldexp(1.0, static_cast<int>(s) - 127);
+}
 
 // bf16 is the upper half of an IEEE binary32: widening is a 16-bit shift.
 float bf16_to_float(uint16_t b) {
@@ -79,20 +106,33 @@ double act_at(const void* base, int dt, size_t idx) {
 // A weight matrix [rows][cols] of one expert, row-major, reduction index
 // contiguous (the nn.Linear "[out][in]" layout).
 struct WeightView {
-  const void* data;      // f32 / bf16 elements, or packed int4 bytes
-  const uint16_t* scale; // int4 only: bf16 [rows][cols/128]
+  const void* data;      // f32 / bf16 / e4m3 elements, or packed int4 / e2m1 bytes
+  const void* scale;     // int4: bf16 [rows][cols/128]; MX: E8M0 bytes [rows][cols/32]
   int dt;
   size_t cols;
   // Decoded element, exactly: for int4, w = q * s with |q| <= 8 and an 8-bit
-  // significand in s, which is exact in binary32 (and in double).
+  // significand in s, which is exact in binary32 (and in double); for MX,
+  // w = element * 2^(s - 127), exact in double.
   double at(size_t r, size_t c) const {
     if (dt == DT_F32) return static_cast<const float*>(data)[r * cols + c];
     if (dt == DT_BF16)
       return bf16_to_float(static_cast<const uint16_t*>(data)[r * cols + c]);
+    if (dt == DT_MXFP8 || dt == DT_MXFP4) {
+      const uint8_t s = static_cast<const uint8_t*>(scale)[r * (cols / kMxBlock) + c / kMxBlock];
+      double v;
+      if (dt == DT_MXFP8) {
+        v = e4m3_value(static_cast<const uint8_t*>(data)[r * cols + c]);
+      } else {
+        const uint8_t byte = static_cast<const uint8_t*>(data)[r * (cols / 2) + c / 2];
+        v = e2m1_value((c & 1) ? (byte >> 4) : (byte & 0x0f));
+      }
+      return v * e8m0_value(s);
+    }
     const uint8_t byte = static_cast<const uint8_t*>(data)[r * (cols / 2) + c / 2];
     const int nib = (c & 1) ? (byte >> 4) : (byte & 0x0f);
     const int q = nib >= 8 ? nib - 16 : nib;
-    const float s = bf16_to_float(scale[r * (cols / kGroup) + c / kGroup]);
+    const float s =
+        bf16_to_float(static_cast<const uint16_t*>(scale)[r * (cols / kGroup) + c / kGroup]);
     return static_cast<double>(static_cast<float>(q) * s);
   }
 };
@@ -108,6 +148,12 @@ WeightView expert_view(const void* w, const void* s, int dt, int e, size_t rows,
     v.data = static_cast<const float*>(w) + e * n;
   } else if (dt == DT_BF16) {
     v.data = static_cast<const uint16_t*>(w) + e * n;
+  } else if (dt == DT_MXFP8) {
+    v.data = static_cast<const uint8_t*>(w) + e * n;
+    v.scale = static_cast<const uint8_t*>(s) + e * (n / kMxBlock);
+  } else if (dt == DT_MXFP4) {
+    v.data = static_cast<const uint8_t*>(w) + e * (n / 2);
+    v.scale = static_cast<const uint8_t*>(s) + e * (n / kMxBlock);
   } else {
     v.data = static_cast<const uint8_t*>(w) + e * (n / 2);
     v.scale = static_cast<const uint16_t*>(s) + e * (n / kGroup);
@@ -259,7 +305,14 @@ int oracle_version(void) { return 1; }
 float oracle_bf16_to_float(uint16_t b) { return bf16_to_float(b); }
 uint16_t oracle_float_to_bf16(float f) { return float_to_bf16_rne(f); }
 
-// Decoded weight element (for the int4 pins).
+// One E4M3 / E2M1 / E8M0 code, decoded (for the MX pins).
+double oracle_mx_element(int w_dt, int code) {
+  if (w_dt == DT_MXFP8) return e4m3_value(static_cast<uint8_t>(code));
+  if (w_dt == DT_MXFP4) return e2m1_value(static_cast<uint8_t>(code & 15));
+  return e8m0_value(static_cast<uint8_t>(code));
+}
+
+// Decoded weight element (for the int4 and MX pins).
 double oracle_weight_at(const void* w, const void* s, int w_dt, int e, int rows,
                         int cols, int r, int c) {
   return expert_view(w, s, w_dt, e, rows, cols).at(r, c);
@@ -322,6 +375,7 @@ int oracle_expert_ffn(const void* x_rows, int act_dt, int n_rows, const void* w_
                       int f, double* y_rows) {
   if (n_rows < 0 || d <= 0 || f <= 0 || e < 0 || !y_rows) return -1;
   if (w_dt == DT_I4G128 && (d % kGroup || f % kGroup)) return -1;
+  if ((w_dt == DT_MXFP8 || w_dt == DT_MXFP4) && (d % kMxBlock || f % kMxBlock)) return -1;
   const WeightView wg = expert_view(w_gate, s_gate, w_dt, e, f, d);
   const WeightView wu = expert_view(w_up, s_up, w_dt, e, f, d);
   const WeightView wd = expert_view(w_down, s_down, w_dt, e, d, f);

@@ -212,6 +212,113 @@ def test_quantiser_round_trip():
 
 
 # --------------------------------------------------------------- bf16, merge
+# ------------------------------------------------------------------ MX formats
+def test_e4m3_decode_matches_torch(oracle_mod):
+    """Every E4M3 code decodes to torch's float8_e4m3fn value (NaN codes NaN)."""
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle_mod.mx_element(inputs.MXFP8, c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_e2m1_and_e8m0_decode_match_the_format_tables(oracle_mod):
+    """E2M1 codes 0..15 against the value table of the OCP MX format (sign
+    bit 3), and E8M0 codes against 2^(c - 127) with 255 = NaN."""
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    want = table + [-v for v in table]
+    got = [oracle_mod.mx_element(inputs.MXFP4, c) for c in range(16)]
+    assert got == want
+    assert math.copysign(1.0, got[8]) == -1.0          # code 8 is -0
+    for c in (0, 1, 100, 127, 128, 200, 254):
+        assert oracle_mod.mx_element(inputs.F32, c) == math.ldexp(1.0, c - 127)
+    assert math.isnan(oracle_mod.mx_element(inputs.F32, 255))
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+def test_mx_weight_decode_is_element_times_scale(oracle_mod, fmt):
+    """weight_at of packed MX weights = element value x 2^(s - 127), with the
+    E2M1 nibble order low = even index and one scale per 32 indices."""
+    rng = np.random.default_rng(7)
+    rows, cols = 3, 96
+    if fmt == "mxfp8":
+        codes = rng.integers(0, 256, size=(1, rows, cols), dtype=np.uint8)
+        codes[codes & 0x7F == 0x7F] = 0x11            # no NaN codes
+        elem = lambda r, c: oracle_mod.mx_element(inputs.MXFP8, codes[0, r, c])  # noqa: E731
+        code = inputs.MXFP8
+    else:
+        nib = rng.integers(0, 16, size=(rows, cols), dtype=np.uint8)
+        codes = (nib[:, 0::2] | (nib[:, 1::2] << 4))[None].astype(np.uint8)
+        elem = lambda r, c: [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0][nib[r, c] & 7] * (  # noqa: E731
+            -1.0 if nib[r, c] & 8 else 1.0)
+        code = inputs.MXFP4
+    scales = rng.integers(100, 140, size=(1, rows, cols // 32), dtype=np.uint8)
+    for r in range(rows):
+        for c in range(0, cols, 7):
+            want = elem(r, c) * 2.0 ** (int(scales[0, r, c // 32]) - 127)
+            assert oracle_mod.weight_at(codes, scales, code, 0, rows, cols, r, c) == want
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+def test_mx_quantiser_round_trip_and_ties(oracle_mod, fmt):
+    """The harness quantiser: decoded weights within half an element step of
+    the input clipped to the format's largest normal (the shared exponent
+    floor(log2 max|w|) - emax lets a block maximum reach just under 2^(emax+1),
+    above 448 or 6), and exact midpoints go to the even code."""
+    g = torch.Generator().manual_seed(8)
+    w = torch.randn(6, 128, generator=g) * 0.02
+    q, s = inputs.quantize_mx(w, fmt)
+    code = inputs.DTYPE_CODE[fmt]
+    wq = q.numpy()[None]
+    sc = s.numpy()[None]
+    mant = 3 if fmt == "mxfp8" else 1
+    for r in range(6):
+        for c in range(128):
+            deq = oracle_mod.weight_at(wq, sc, code, 0, 6, 128, r, c)
+            scale = 2.0 ** (int(sc[0, r, c // 32]) - 127)
+            top = 448.0 if fmt == "mxfp8" else 6.0
+            x = math.copysign(min(abs(float(w[r, c])), top * scale), float(w[r, c]))
+            a = abs(x) / scale
+            step = 2.0 ** (max(math.floor(math.log2(a)), 0 if fmt == "mxfp4" else -6) - mant) \
+                if a > 0 else 0.0
+            assert abs(deq - x) <= step / 2 * scale * (1 + 1e-12) + 1e-30
+    # ties: in block units, E2M1 1.25 (between 1 and 1.5) -> 1 (even code 2),
+    # 1.75 -> 2; E4M3 1.0625 (between 1 and 1.125) -> 1, 1.1875 -> 1.25
+    vals = [1.25, 1.75, 2.5, 5.0] if fmt == "mxfp4" else [1.0625, 1.1875, 17.0, 19.0]
+    want = [1.0, 2.0, 2.0, 4.0] if fmt == "mxfp4" else [1.0, 1.25, 16.0, 20.0]
+    row = torch.zeros(1, 32)
+    row[0, :4] = torch.tensor(vals)
+    row[0, 31] = 6.0 if fmt == "mxfp4" else 448.0   # fixes the block exponent at 0
+    q, s = inputs.quantize_mx(row, fmt)
+    assert int(s[0, 0]) == 127
+    got = [oracle_mod.weight_at(q.numpy()[None], s.numpy()[None], code, 0, 1, 32, 0, c)
+           for c in range(4)]
+    assert got == want
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+def test_mx_ffn_equals_f32_ffn_on_decoded_weights(oracle_mod, fmt):
+    s = inputs.MoEShape("mx", T=5, d=128, E=2, k=1, f=64, wdt=fmt)
+    lay = inputs.make_layer(s, seed=18)
+    code = inputs.DTYPE_CODE[fmt]
+    dec = {}
+    for key, rows, cols in (("w_gate", s.f, s.d), ("w_up", s.f, s.d), ("w_down", s.d, s.f)):
+        skey = "s_" + key[2:]
+        m = np.zeros((s.E, rows, cols), np.float32)
+        for e in range(s.E):
+            for r in range(rows):
+                for c in range(cols):
+                    m[e, r, c] = oracle_mod.weight_at(lay[key], lay[skey], code, e, rows, cols,
+                                                      r, c)
+        dec[key] = torch.from_numpy(m)
+    x = lay["x"]
+    for e in range(s.E):
+        got = oracle_mod.expert_ffn(x, s.act_code, lay, e, s.d, s.f, code)
+        ref = oracle_mod.expert_ffn(x, s.act_code, dec, e, s.d, s.f, inputs.F32)
+        assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
 def test_bf16_rounding_matches_torch(oracle_mod):
     vals = [0.0, -0.0, 1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 2 ** -8 + 2 ** -20,
             -2.5e-3, 3.4e38, 1e-40, float("inf"), -float("inf")]
