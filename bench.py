@@ -302,6 +302,10 @@ def roofline(s, path, n_rows, active, avg, ms_fwd, pk, pk_src, config_name):
         if s.wdt == "i4g128":
             per_expert = 2 * s.f * s.d // 2 + 2 * s.f * (s.d // 128) * 2
             all_bytes = active * (3 * s.f * s.d // 2 + 3 * s.f * (s.d // 128) * 2)
+        elif s.wdt in ("mxfp8", "mxfp4"):
+            per = 1 if s.wdt == "mxfp8" else 2    # elements per byte
+            per_expert = 2 * s.f * s.d // per + 2 * s.f * (s.d // 32)
+            all_bytes = active * (3 * s.f * s.d // per + 3 * s.f * (s.d // 32))
         else:
             wsz = 4 if s.wdt == "f32" else 2
             per_expert = 2 * s.f * s.d * wsz
@@ -311,7 +315,9 @@ def roofline(s, path, n_rows, active, avg, ms_fwd, pk, pk_src, config_name):
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"],
                 "traffic": traffic_record(config_name, "dec"),
-                "kernel": "k_dec_gateup (expert gate/up projection + SwiGLU)",
+                "kernel": ("k_mx_gateup (MX expert gate/up projection + SwiGLU)"
+                           if s.wdt in ("mxfp8", "mxfp4") else
+                           "k_dec_gateup (expert gate/up projection + SwiGLU)"),
                 "algorithmic_bytes_per_launch": alg,
                 "unit_work": f"{per_expert} B of gate/up weights per activated expert x "
                              f"{active} activated experts",
@@ -350,6 +356,8 @@ def roofline(s, path, n_rows, active, avg, ms_fwd, pk, pk_src, config_name):
     # bf16/int4 experts reads token rows of x directly and writes no x_perm
     asz = 4 if s.act == "f32" else 2
     xperm = 0 if (path == "decode" and s.wdt != "f32") else 2 * n_rows * s.d * asz
+    if s.wdt in ("mxfp8", "mxfp4"):
+        xperm = 2 * s.T * s.d * 2  # the fp16 copy of the token rows
     roof["overhead_bytes"] = {
         "x_perm": xperm, "H": 2 * n_rows * s.f * (4 if s.wdt == "f32" else 2),
         "y_perm": 2 * n_rows * s.d * 4}
@@ -496,15 +504,17 @@ def measure(s, steps, warmup, world, rank, local, cpu_seconds, with_e2e=True,
 
 # the other workloads measured beside the headline one in a default run:
 # the remaining configurations, then one int4 layer at a prefill batch
-EXTRA = ["mixtral_prefill", "fine_int4", "skewed", "tiny_fp32", "mixtral_prefill_int4"]
+EXTRA = ["mixtral_prefill", "fine_int4", "skewed", "tiny_fp32", "mixtral_prefill_int4",
+         "mixtral_decode_mxfp8", "fine_mxfp4"]
 
 
 def sub_steps(s, K: int) -> int:
     """Timed forwards for a non-headline workload: at least K, and enough
     for about 0.3 s of timed work (capped), from a rough cost model."""
     flops = 2.0 * s.T * s.k * 3 * s.d * s.f
-    est_ms = max(0.02, flops / 1.2e15 * 1e3, 3 * s.d * s.f * min(s.E, s.T * s.k) *
-                 (0.53 if s.wdt == "i4g128" else 2.0) / 5.0e12 * 1e3)
+    bpw = {"i4g128": 0.53, "mxfp8": 1.03, "mxfp4": 0.53}.get(s.wdt, 2.0)  # bytes per weight
+    est_ms = max(0.02, flops / 1.2e15 * 1e3,
+                 3 * s.d * s.f * min(s.E, s.T * s.k) * bpw / 5.0e12 * 1e3)
     return int(max(K, min(400, 300.0 / est_ms)))
 
 

@@ -61,13 +61,30 @@ typedef enum {
   COLI_ETIMEOUT = -6      /* a bounded device-side wait ran out */
 } coli_status;
 
-typedef enum { COLI_F32 = 0, COLI_BF16 = 1, COLI_I4G128 = 2 } coli_dtype;
+/* Expert weight formats beyond f32/bf16:
+ *   COLI_I4G128: signed int4 nibbles, bf16 scale per 128 reduction indices;
+ *   COLI_MXFP8:  OCP Microscaling E4M3 bytes [..][cols], one E8M0 scale byte
+ *                (2^(s-127)) per 32 reduction indices [..][cols/32];
+ *   COLI_MXFP4:  OCP Microscaling E2M1 nibbles [..][cols/2] (low nibble = even
+ *                index), E8M0 scale bytes [..][cols/32].
+ * MX formats are the block-scaled low-precision weights of the model families
+ * in the wth2jhl.online deep dive's table (MXFP4, FP8); they run on the
+ * decode path with fp16 activations (values beyond the fp16 range are
+ * saturated and latch COLI_EDEVICE). */
+typedef enum {
+  COLI_F32 = 0,
+  COLI_BF16 = 1,
+  COLI_I4G128 = 2,
+  COLI_MXFP8 = 3,
+  COLI_MXFP4 = 4
+} coli_dtype;
 
 /* Expert-FFN path. AUTO picks DECODE when the mean number of rows per expert
  * (T*k/E) is at most 64, else PREFILL. DECODE streams each active expert's
  * weights once (tensor-core MMA fed straight from HBM); PREFILL is the
  * TMA + tcgen05/TMEM grouped GEMM. Both give the same routing and the same
- * outputs within rounding. F32 layers always use the CUDA-core path.
+ * outputs within rounding. F32 layers always use the CUDA-core path; MX
+ * layers always use DECODE (PREFILL is COLI_EUNSUPPORTED for them).
  * int4 experts run on both: DECODE applies each group's scale to the exact
  * sum of q*x in fp32 (w = q*s exactly); PREFILL dequantises each weight to a
  * bf16 tensor-core operand, q*s rounded once to nearest even (q*s can need 11
@@ -82,7 +99,8 @@ typedef struct {
   int32_t top_k;           /* k: 1..min(E, 8) */
   int32_t max_tokens;      /* largest T any forward will see (workspace size) */
   int32_t act_dtype;       /* coli_dtype of x, y and W_r: F32 or BF16 */
-  int32_t weight_dtype;    /* F32 (with F32 activations), BF16 or I4G128 (with BF16) */
+  int32_t weight_dtype;    /* F32 (with F32 activations); BF16, I4G128, MXFP8 or MXFP4
+                              (with BF16) */
   int32_t has_router_bias; /* 0 or 1 */
   int32_t path;            /* coli_path */
 } coli_moe_config;
@@ -90,12 +108,12 @@ typedef struct {
 typedef struct {
   const void* w_router;  /* [E][d] act dtype */
   const float* b_router; /* [E] f32, or NULL when has_router_bias == 0 */
-  const void* w_gate;    /* [E][f][d]   (int4: [E][f][d/2] bytes) */
-  const void* w_up;      /* [E][f][d]   (int4: [E][f][d/2] bytes) */
-  const void* w_down;    /* [E][d][f]   (int4: [E][d][f/2] bytes) */
-  const void* s_gate;    /* int4 only: bf16 [E][f][d/128], else NULL */
-  const void* s_up;      /* int4 only: bf16 [E][f][d/128], else NULL */
-  const void* s_down;    /* int4 only: bf16 [E][d][f/128], else NULL */
+  const void* w_gate;    /* [E][f][d]   (int4, MXFP4: [E][f][d/2] bytes; MXFP8: bytes) */
+  const void* w_up;      /* [E][f][d]   (as w_gate) */
+  const void* w_down;    /* [E][d][f]   (int4, MXFP4: [E][d][f/2] bytes; MXFP8: bytes) */
+  const void* s_gate;    /* int4: bf16 [E][f][d/128]; MX: u8 [E][f][d/32]; else NULL */
+  const void* s_up;      /* as s_gate */
+  const void* s_down;    /* int4: bf16 [E][d][f/128]; MX: u8 [E][d][f/32]; else NULL */
 } coli_moe_weights;
 
 typedef struct coli_moe coli_moe;

@@ -15,7 +15,7 @@ import os
 import re
 import threading
 
-F32, BF16, I4G128 = 0, 1, 2
+F32, BF16, I4G128, MXFP8, MXFP4 = 0, 1, 2, 3, 4
 PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
 STATUS = {0: "COLI_OK", -1: "COLI_EINVAL", -2: "COLI_ENOMEM", -3: "COLI_ECUDA",
           -4: "COLI_EUNSUPPORTED", -5: "COLI_EDEVICE", -6: "COLI_ETIMEOUT"}

@@ -174,10 +174,18 @@ int validate_cfg(const coli_moe_config* c, char* err, size_t err_len) {
   if (c->act_dtype == COLI_F32 && c->weight_dtype != COLI_F32)
     return fail(err, err_len, COLI_EINVAL, "F32 activations need F32 expert weights");
   if (c->act_dtype == COLI_BF16 && c->weight_dtype != COLI_BF16 &&
-      c->weight_dtype != COLI_I4G128)
-    return fail(err, err_len, COLI_EINVAL, "BF16 activations need BF16 or I4G128 weights");
+      c->weight_dtype != COLI_I4G128 && c->weight_dtype != COLI_MXFP8 &&
+      c->weight_dtype != COLI_MXFP4)
+    return fail(err, err_len, COLI_EINVAL,
+                "BF16 activations need BF16, I4G128, MXFP8 or MXFP4 weights");
   if (c->weight_dtype == COLI_I4G128 && (c->d_model % 128 || c->d_ff % 128))
     return fail(err, err_len, COLI_EINVAL, "int4 groups need d_model and d_ff multiples of 128");
+  if ((c->weight_dtype == COLI_MXFP8 || c->weight_dtype == COLI_MXFP4) &&
+      (c->d_model % 128 || c->d_ff % 128))
+    return fail(err, err_len, COLI_EINVAL, "MX weights need d_model and d_ff multiples of 128");
+  if ((c->weight_dtype == COLI_MXFP8 || c->weight_dtype == COLI_MXFP4) &&
+      c->path == COLI_PATH_PREFILL)
+    return fail(err, err_len, COLI_EUNSUPPORTED, "MX weights run on the decode path only");
   if (c->path < COLI_PATH_AUTO || c->path > COLI_PATH_PREFILL)
     return fail(err, err_len, COLI_EINVAL, "unknown path %d", c->path);
   return COLI_OK;
@@ -246,6 +254,30 @@ int run_ffn(coli_moe* h, const void* x_perm, const int32_t* offsets, int n_rows,
     if (y_bf16) *y_bf16 = allow_bf16;
     timing_mark(h, ts, 4, st);
     *launches += 2;
+    return COLI_OK;
+  }
+  const int steps_mx = f / 128;
+  if (c.weight_dtype == COLI_MXFP8 || c.weight_dtype == COLI_MXFP4) {
+    // fp16 activations (token rows, or the caller's permuted rows) in the
+    // handle's x_perm buffer, which this path leaves unused otherwise
+    const void* xa = row_token ? x_tok : x_perm;
+    const int xa_rows = row_token ? T : n_rows;
+    CUDA_TRY(launch_to_f16(xa, static_cast<size_t>(xa_rows) * d, h->x_perm, st, status));
+    CUDA_TRY(launch_mx_gateup(h->w, h->x_perm, row_token, offsets, E, d, f, h->H, h->dec_grid,
+                              st, status));
+    timing_mark(h, ts, 3, st);
+    int max_splits = kSplitRows / n_rows;
+    if (max_splits > kMaxSplits) max_splits = kMaxSplits;
+    const int splits = dec_down_splits(n_rows, E, d, steps_mx, h->dec_grid * 8, max_splits);
+    if (splits > 1)
+      CUDA_TRY(launch_mx_down(h->w, h->H, offsets, E, d, f, splits, h->y_part,
+                              static_cast<size_t>(n_rows) * d, h->dec_grid, st, status));
+    else
+      CUDA_TRY(launch_mx_down(h->w, h->H, offsets, E, d, f, 1, static_cast<float*>(y_perm), 0,
+                              h->dec_grid, st, status));
+    timing_mark(h, ts, 4, st);
+    *launches += 3;
+    *splits_out = splits;
     return COLI_OK;
   }
   // gate/up activations: token rows of x through row_token (no x_perm), or
@@ -320,8 +352,9 @@ int coli_moe_create(const coli_moe_config* cfg, const coli_moe_weights* wts, voi
   if (cfg->has_router_bias && !wts->b_router)
     return fail(err, err_len, COLI_EINVAL, "has_router_bias=1 but b_router is NULL");
   const bool i4 = cfg->weight_dtype == COLI_I4G128;
-  if (i4 && (!wts->s_gate || !wts->s_up || !wts->s_down))
-    return fail(err, err_len, COLI_EINVAL, "int4 weights need s_gate, s_up and s_down");
+  const bool mx = cfg->weight_dtype == COLI_MXFP8 || cfg->weight_dtype == COLI_MXFP4;
+  if ((i4 || mx) && (!wts->s_gate || !wts->s_up || !wts->s_down))
+    return fail(err, err_len, COLI_EINVAL, "int4 and MX weights need s_gate, s_up and s_down");
   const void* ptrs[] = {wts->w_router, wts->w_gate, wts->w_up, wts->w_down};
   for (const void* p : ptrs)
     if (!aligned16(p)) return fail(err, err_len, COLI_EINVAL, "weight buffers must be 16-byte aligned");
@@ -340,7 +373,7 @@ int coli_moe_create(const coli_moe_config* cfg, const coli_moe_weights* wts, voi
   if ((e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device)) !=
       cudaSuccess)
     return bail(COLI_ECUDA, "device attributes", e);
-  h->dec_grid = h->num_sms * dec_blocks_per_sm();
+  h->dec_grid = h->num_sms * (mx ? mx_blocks_per_sm(cfg->weight_dtype) : dec_blocks_per_sm());
   if (device_status_ptr() == nullptr) return bail(COLI_ECUDA, "status word", cudaGetLastError());
 
   // weights
@@ -351,6 +384,12 @@ int coli_moe_create(const coli_moe_config* cfg, const coli_moe_weights* wts, voi
     dn_bytes = static_cast<size_t>(E) * d * f / 2;
     sgu_bytes = static_cast<size_t>(E) * 2 * f * (d / 128) * 2;
     sdn_bytes = static_cast<size_t>(E) * d * (f / 128) * 2;
+  } else if (mx) {
+    const size_t per = cfg->weight_dtype == COLI_MXFP8 ? 1 : 2;  // elements per byte
+    gu_bytes = static_cast<size_t>(E) * 2 * f * d / per;
+    dn_bytes = static_cast<size_t>(E) * d * f / per;
+    sgu_bytes = static_cast<size_t>(E) * 2 * f * (d / 32);
+    sdn_bytes = static_cast<size_t>(E) * d * (f / 32);
   } else {
     const size_t wsz = cfg->weight_dtype == COLI_F32 ? 4 : 2;
     gu_bytes = static_cast<size_t>(E) * 2 * f * d * wsz;
@@ -395,16 +434,19 @@ int coli_moe_create(const coli_moe_config* cfg, const coli_moe_weights* wts, voi
       (e = cudaMemcpyAsync(h->b_router, wts->b_router, E * sizeof(float), cudaMemcpyDefault,
                            st)) != cudaSuccess)
     return bail(COLI_ECUDA, "copy router bias", e);
-  if ((e = launch_repack(wts->w_gate, wts->w_up, wts->w_down, wts->s_gate, wts->s_up,
-                         wts->s_down, cfg->weight_dtype, E, d, f, wgu, sgu, wdn, sdn, st)) !=
-      cudaSuccess)
-    return bail(COLI_ECUDA, "repack expert weights", e);
+  e = mx ? launch_repack_mx(wts->w_gate, wts->w_up, wts->w_down, wts->s_gate, wts->s_up,
+                           wts->s_down, cfg->weight_dtype, E, d, f, wgu, sgu, wdn, sdn, st)
+         : launch_repack(wts->w_gate, wts->w_up, wts->w_down, wts->s_gate, wts->s_up,
+                         wts->s_down, cfg->weight_dtype, E, d, f, wgu, sgu, wdn, sdn, st);
+  if (e != cudaSuccess) return bail(COLI_ECUDA, "repack expert weights", e);
   h->w.wdt = cfg->weight_dtype;
   h->w.w_gu = wgu;
   h->w.w_dn = wdn;
+  h->w.s_gu_u8 = mx ? static_cast<const uint8_t*>(sgu) : nullptr;
+  h->w.s_dn_u8 = mx ? static_cast<const uint8_t*>(sdn) : nullptr;
   h->w.s_gu = static_cast<const __nv_bfloat16*>(sgu);
   h->w.s_dn = static_cast<const __nv_bfloat16*>(sdn);
-  if (cfg->weight_dtype != COLI_F32 && tc_supported(d, f)) {
+  if ((cfg->weight_dtype == COLI_BF16 || i4) && tc_supported(d, f)) {
     if ((e = tc_plan_create(&h->tc, cfg->weight_dtype, wgu, wdn, h->w.s_gu, h->w.s_dn, E, d, f,
                             static_cast<int>(Na), h->x_perm, h->H)) != cudaSuccess)
       return bail(COLI_ECUDA, "tensor-core plan", e);

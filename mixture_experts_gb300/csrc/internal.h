@@ -9,7 +9,7 @@
 
 namespace coli {
 
-enum { DT_F32 = 0, DT_BF16 = 1, DT_I4G128 = 2 };
+enum { DT_F32 = 0, DT_BF16 = 1, DT_I4G128 = 2, DT_MXFP8 = 3, DT_MXFP4 = 4 };
 
 // Stores msg as the calling thread's coli_last_error() text; returns code.
 int record_error(int code, const char* msg);
@@ -47,9 +47,11 @@ cudaError_t launch_permute(const int32_t* topk_idx, const void* x, int T, int d,
 struct FfnWeights {
   int wdt;
   const void* w_gu;
-  const __nv_bfloat16* s_gu;
+  const __nv_bfloat16* s_gu;  // int4 scales
   const void* w_dn;
   const __nv_bfloat16* s_dn;
+  const uint8_t* s_gu_u8;     // MX: E8M0 scale bytes [rows][K/32]
+  const uint8_t* s_dn_u8;
 };
 
 // Tensor-core decode path: streams the weights of every non-empty expert once.
@@ -74,6 +76,23 @@ int dec_blocks_per_sm();
 cudaError_t launch_f32_ffn(const float* w_gu, const float* w_dn, const float* x_perm,
                            const int32_t* offsets, int n_rows, int E, int d, int f, float* H,
                            float* y_perm, cudaStream_t st, int* n_launches);
+
+// Block-scaled (MX) experts, decode path: fp16 activations x16 ([T][d]
+// through row_token, or [rows][d]), H16 [rows][f] fp16 written by gate/up.
+// Values beyond the fp16 range are saturated and latch COLI_EDEVICE.
+int mx_blocks_per_sm(int wdt);
+cudaError_t launch_to_f16(const void* x_bf16, size_t n, void* x_f16, cudaStream_t st,
+                          int* status);
+cudaError_t launch_mx_gateup(const FfnWeights& w, const void* x16, const int32_t* row_token,
+                             const int32_t* offsets, int E, int d, int f, void* H16, int grid,
+                             cudaStream_t st, int* status);
+cudaError_t launch_mx_down(const FfnWeights& w, const void* H16, const int32_t* offsets, int E,
+                           int d, int f, int splits, float* y_part, size_t part_stride, int grid,
+                           cudaStream_t st, int* status);
+cudaError_t launch_repack_mx(const void* src_gate, const void* src_up, const void* src_down,
+                             const void* sg, const void* su, const void* sd, int wdt, int E,
+                             int d, int f, void* dst_gu, void* dst_sgu, void* dst_dn,
+                             void* dst_sdn, cudaStream_t st);
 
 // Prefill path: TMA + tcgen05/TMEM grouped GEMM (bf16 or int4 weights).
 struct TcPlan;  // defined in k_ffn_tc.cu

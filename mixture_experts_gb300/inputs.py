@@ -95,9 +95,13 @@ CONFIGS = {
     "fine_int4": MoEShape("fine_int4", T=256, d=6144, E=256, k=8, f=2048, wdt="i4g128"),
     "skewed": MoEShape("skewed", T=16384, d=2048, E=64, k=4, f=1408, bias="zipf"),
     # beside the five: the Mixtral-shaped prefill layer with int4 g128
-    # experts (~1024 rows per expert), for the int4 tensor-core GEMM
+    # experts (~1024 rows per expert), for the int4 tensor-core GEMM; and the
+    # two decode layers with block-scaled (OCP MX) experts
     "mixtral_prefill_int4": MoEShape("mixtral_prefill_int4", T=4096, d=4096, E=8, k=2,
                                      f=14336, wdt="i4g128"),
+    "mixtral_decode_mxfp8": MoEShape("mixtral_decode_mxfp8", T=32, d=4096, E=8, k=2, f=14336,
+                                     wdt="mxfp8"),
+    "fine_mxfp4": MoEShape("fine_mxfp4", T=256, d=6144, E=256, k=8, f=2048, wdt="mxfp4"),
 }
 
 

@@ -10,7 +10,7 @@ import oracle
 from mixture_experts_gb300 import inputs
 
 # max|err| / max|ref| bounds on the layer output per expert weight type
-TOL = {"f32": 1e-5, "bf16": 2e-2, "i4g128": 3e-2}
+TOL = {"f32": 1e-5, "bf16": 2e-2, "i4g128": 3e-2, "mxfp8": 3e-2, "mxfp4": 3e-2}
 GATE_TOL = 1e-6   # absolute, on the renormalised gates
 NEAR_TIE = 1e-5   # fp32 logit gap below which several selections are correct
 

@@ -46,6 +46,19 @@ def test_create_rejects_int4_with_bad_group(lib):
     assert rc == moe.COLI_EINVAL and "128" in msg
 
 
+@pytest.mark.parametrize("wdt", [moe.MXFP8, moe.MXFP4])
+def test_create_rejects_mx_shapes_and_prefill(lib, wdt):
+    cfg = moe.coli_moe_config(192, 512, 8, 2, 16, moe.BF16, wdt, 0, 0)
+    rc, _, msg = moe.coli_moe_create(cfg, moe.coli_moe_weights(), stream=0)
+    assert rc == moe.COLI_EINVAL and "128" in msg
+    cfg = moe.coli_moe_config(256, 512, 8, 2, 16, moe.BF16, wdt, 0, moe.PATH_PREFILL)
+    rc, _, msg = moe.coli_moe_create(cfg, moe.coli_moe_weights(), stream=0)
+    assert rc == moe.COLI_EUNSUPPORTED and "decode" in msg
+    cfg = moe.coli_moe_config(256, 512, 8, 2, 16, moe.F32, wdt, 0, 0)
+    rc, _, msg = moe.coli_moe_create(cfg, moe.coli_moe_weights(), stream=0)
+    assert rc == moe.COLI_EINVAL
+
+
 def test_create_rejects_missing_weights(lib):
     cfg = moe.coli_moe_config(256, 512, 8, 2, 16, moe.BF16, moe.BF16, 0, 0)
     rc, _, msg = moe.coli_moe_create(cfg, moe.coli_moe_weights(), stream=0)

@@ -101,6 +101,21 @@ def test_nan_router_row_still_gives_k_distinct_ids(E, k):
     assert moe.coli_device_status() == moe.COLI_OK
 
 
+def test_mx_activation_beyond_fp16_is_saturated_and_latched():
+    """MX experts take fp16 activations: a bf16 input above the fp16 range is
+    saturated (no inf reaches the output) and latches a data error."""
+    assert moe.coli_device_status() == moe.COLI_OK
+    s = inputs.MoEShape("mxbig", T=8, d=256, E=4, k=2, f=128, wdt="mxfp8")
+    lay = inputs.make_layer(s, seed=9)
+    lay["x"][2, 5] = 1.0e6
+    dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in lay.items()}
+    layer = moe.MoELayer(s.d, s.f, s.E, s.k, s.T, s.act_code, s.w_code, dev)
+    y = layer(dev["x"])
+    assert layer.status() == moe.COLI_EDEVICE
+    assert torch.isfinite(y.float()).all()
+    assert layer.status() == moe.COLI_OK
+
+
 def test_bounded_wait_times_out_and_context_survives():
     assert moe.coli_device_status() == moe.COLI_OK
     assert moe.coli_selftest_bounded_wait(2000) == moe.COLI_OK

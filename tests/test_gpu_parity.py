@@ -30,6 +30,11 @@ SMALL = {
     # int4 experts with hundreds of rows each: the tcgen05 grouped GEMM with
     # the weights dequantised in shared memory
     "int4_prefill": S("int4_prefill", T=600, d=512, E=4, k=2, f=384, wdt="i4g128"),
+    # block-scaled experts (decode path, fp16 MMAs): one and two token tiles
+    # per pass, several passes per expert
+    "mxfp8": S("mxfp8", T=40, d=512, E=8, k=2, f=256, wdt="mxfp8"),
+    "mxfp4": S("mxfp4", T=60, d=384, E=6, k=3, f=384, wdt="mxfp4"),
+    "mxfp8_bias": S("mxfp8_bias", T=90, d=256, E=16, k=4, f=128, wdt="mxfp8", bias="zipf"),
 }
 
 
@@ -123,6 +128,17 @@ def test_full_config(name):
     err, near = check_layer(s, lay, y, dbg, threads=os.cpu_count() or 1)
     print(f"{name}: path={layer.path_for(s.T)} rel_err={err:.3e} near_ties={near} "
           f"tokens_checked={s.T - near}")
+
+
+@pytest.mark.parametrize("name", ["mixtral_decode_mxfp8", "fine_mxfp4"])
+def test_full_mx_layers(name):
+    """The decode layers with MX experts at full size: every token."""
+    s = inputs.CONFIGS[name]
+    lay = inputs.make_layer(s, seed=0)
+    layer, y, dbg = run_layer(s, lay)
+    assert layer.path_for(s.T) == moe.PATH_DECODE
+    err, near = check_layer(s, lay, y, dbg, threads=os.cpu_count() or 1)
+    print(f"{name}: rel_err={err:.3e} near_ties={near} tokens_checked={s.T - near}")
 
 
 def test_full_int4_prefill_layer_sampled():
@@ -243,7 +259,7 @@ def test_stage_permute_without_row_copy(T, E, k):
     assert moe.coli_device_status() == 0
 
 
-@pytest.mark.parametrize("name", ["decode_bf16", "int4", "tiny_fp32"])
+@pytest.mark.parametrize("name", ["decode_bf16", "int4", "tiny_fp32", "mxfp8", "mxfp4"])
 def test_stage_expert_ffn(name):
     s = SMALL[name]
     lay, dev = _stage_layer(s, 31)
