@@ -52,7 +52,36 @@ struct FfnWeights {
   const __nv_bfloat16* s_dn;
   const uint8_t* s_gu_u8;     // MX: E8M0 scale bytes [rows][K/32]
   const uint8_t* s_dn_u8;
+  // Residency tier (decode path): per-expert device arrays [E] with the base
+  // of each expert's weights / scales (an HBM slot or mapped host memory);
+  // nullptr when every expert is resident at w_gu + e * (expert bytes).
+  const uint8_t* const* tab_gu;
+  const uint8_t* const* tab_dn;
+  const uint8_t* const* tab_sgu;
+  const uint8_t* const* tab_sdn;
 };
+
+// Expert residency tier state (device pointers; host_* point at mapped
+// pinned host memory). Byte counts are per expert.
+struct ResidencyState {
+  float* score;         // [E] routing score
+  int32_t* slot_of;     // [E] slot holding expert e, or -1
+  int32_t* expert_in;   // [S] expert held by a slot, or -1
+  int32_t* copy_list;   // [2 P] (expert, slot) pairs of this update
+  int32_t* n_copy;      // [1]
+  int32_t* promotions;  // [1] running count
+  const uint8_t** tab_gu;
+  const uint8_t** tab_dn;
+  const uint8_t** tab_sgu;
+  const uint8_t** tab_sdn;
+  uint8_t *host_gu, *host_dn, *host_sgu, *host_sdn;
+  uint8_t *slot_gu, *slot_dn, *slot_sgu, *slot_sdn;
+  size_t gu_bytes, dn_bytes, sgu_bytes, sdn_bytes;
+};
+// After a forward: scores from this forward's counts, up to P promotions of
+// top-S experts into slots (tables repointed, weights copied host -> slot).
+cudaError_t launch_residency_update(const int32_t* counts, int E, int S, int P,
+                                    const ResidencyState& R, int grid, cudaStream_t st);
 
 // Tensor-core decode path: streams the weights of every non-empty expert once.
 // steps = reduction steps of one down row (f/32 bf16, f/128 int4)

@@ -209,6 +209,8 @@ struct DecArgs {
   const float* xsum;             // int4: 136 * per-group sums of the activation rows
   const uint8_t* w;              // gate/up or down weights (bytes)
   const __nv_bfloat16* s;        // int4 scales or nullptr
+  const uint8_t* const* wtab;    // residency tier: expert e's weights at wtab[e], or nullptr
+  const uint8_t* const* stab;    // ... and its int4 scales at stab[e]
   const __nv_bfloat16* x;        // activations [rows][K] (x_perm or H), or x [T][K]
   const int32_t* row_token;      // non-null: row r reads x[row_token[r]] (and its xsum row)
   const int32_t* offsets;        // [E+1]
@@ -235,16 +237,21 @@ COLI_DEV void gateup_chunk(const DecArgs& A, const int32_t* tok, int e, int n0, 
   const size_t rb = row_bytes<INT4>(A.K);
   const int gs = A.K / 128;
   // interleaved rows: gate feature n -> 128*(n/64) + n%64, up -> +64
-  const size_t gbase = static_cast<size_t>(e) * A.rows_per_expert + 128 * (n0 / 64) + (n0 % 64);
+  const size_t gin = 128 * (n0 / 64) + (n0 % 64);  // row within the expert
+  const uint8_t* wbase = A.wtab ? A.wtab[e] : A.w + static_cast<size_t>(e) * A.rows_per_expert * rb;
+  const __nv_bfloat16* sbase =
+      !INT4 ? nullptr
+            : (A.stab ? reinterpret_cast<const __nv_bfloat16*>(A.stab[e])
+                      : A.s + static_cast<size_t>(e) * A.rows_per_expert * gs);
   const uint8_t* wrow[2][2];
   const __nv_bfloat16* srow[2][2];
 #pragma unroll
   for (int m = 0; m < 2; ++m)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const size_t row = gbase + 64 * m + r + 8 * h;
-      wrow[m][h] = A.w + row * rb + q * 16;
-      srow[m][h] = INT4 ? A.s + row * gs : nullptr;
+      const size_t row = gin + 64 * m + r + 8 * h;
+      wrow[m][h] = wbase + row * rb + q * 16;
+      srow[m][h] = INT4 ? sbase + row * gs : nullptr;
     }
   // activation row of token column j: the permuted row, or the token's row of
   // x when the rows are gathered here (the dispatch then copies nothing)
@@ -295,15 +302,20 @@ COLI_DEV void down_chunk(const DecArgs& A, int e, int o0, int split, int row0, i
   const int lane = threadIdx.x & 31, r = lane >> 2, q = lane & 3;
   const size_t rb = row_bytes<INT4>(A.K);
   const int gs = A.K / 128;
+  const uint8_t* wbase = A.wtab ? A.wtab[e] : A.w + static_cast<size_t>(e) * A.rows_per_expert * rb;
+  const __nv_bfloat16* sbase =
+      !INT4 ? nullptr
+            : (A.stab ? reinterpret_cast<const __nv_bfloat16*>(A.stab[e])
+                      : A.s + static_cast<size_t>(e) * A.rows_per_expert * gs);
   const uint8_t* wrow[2][2];
   const __nv_bfloat16* srow[2][2];
 #pragma unroll
   for (int m = 0; m < 2; ++m)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const size_t row = static_cast<size_t>(e) * A.rows_per_expert + o0 + 16 * m + r + 8 * h;
-      wrow[m][h] = A.w + row * rb + q * 16;
-      srow[m][h] = INT4 ? A.s + row * gs : nullptr;
+      const size_t row = static_cast<size_t>(o0) + 16 * m + r + 8 * h;  // within the expert
+      wrow[m][h] = wbase + row * rb + q * 16;
+      srow[m][h] = INT4 ? sbase + row * gs : nullptr;
     }
   const uint8_t* xrow[NT];
   const int xlane = INT4 ? q * 64 : q * 16;
@@ -507,6 +519,8 @@ cudaError_t launch_dec_gateup(const FfnWeights& w, const __nv_bfloat16* x,
   A.xsum = xsum;
   A.w = static_cast<const uint8_t*>(w.w_gu);
   A.s = w.s_gu;
+  A.wtab = w.tab_gu;
+  A.stab = w.tab_sgu;
   A.x = x;
   A.row_token = row_token;
   A.offsets = offsets;
@@ -529,6 +543,8 @@ cudaError_t launch_dec_down(const FfnWeights& w, const __nv_bfloat16* H, const i
   A.xsum = hsum;
   A.w = static_cast<const uint8_t*>(w.w_dn);
   A.s = w.s_dn;
+  A.wtab = w.tab_dn;
+  A.stab = w.tab_sdn;
   A.x = H;
   A.offsets = offsets;
   A.E = E;

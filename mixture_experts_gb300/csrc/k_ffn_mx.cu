@@ -187,6 +187,8 @@ COLI_DEV void mx_mainloop(const uint8_t* const (&wrow)[2][2], const uint32_t* co
 struct MxArgs {
   const uint8_t* w;          // repacked weights (gate/up or down)
   const uint8_t* s;          // E8M0 scales [weight rows][K/32]
+  const uint8_t* const* wtab;  // residency tier: expert e's weights at wtab[e], or nullptr
+  const uint8_t* const* stab;  // ... and its scales at stab[e]
   const __half* x;           // fp16 activations: [T][K] through row_token, or [rows][K]
   const int32_t* row_token;  // non-null: row r reads x[row_token[r]]
   const int32_t* offsets;    // [E+1]
@@ -210,16 +212,19 @@ COLI_DEV void mx_gateup_chunk(const MxArgs& A, const int32_t* tok, int e, int n0
   const int lane = threadIdx.x & 31, r = lane >> 2, q = lane & 3;
   const size_t rb = mx_row_bytes<FMT>(A.K);
   const int sw = A.K / 128;  // scale words per row
-  const size_t gbase = static_cast<size_t>(e) * A.rows_per_expert + 128 * (n0 / 64) + (n0 % 64);
+  const size_t gin = 128 * (n0 / 64) + (n0 % 64);  // row within the expert
+  const size_t e0 = static_cast<size_t>(e) * A.rows_per_expert;
+  const uint8_t* wbase = A.wtab ? A.wtab[e] : A.w + e0 * rb;
+  const uint32_t* sbase = reinterpret_cast<const uint32_t*>(A.stab ? A.stab[e] : A.s + e0 * sw * 4);
   const uint8_t* wrow[2][2];
   const uint32_t* srow[2][2];
 #pragma unroll
   for (int m = 0; m < 2; ++m)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const size_t row = gbase + 64 * m + r + 8 * h;
-      wrow[m][h] = A.w + row * rb + q * kLaneStep<FMT>;
-      srow[m][h] = reinterpret_cast<const uint32_t*>(A.s) + row * sw;
+      const size_t row = gin + 64 * m + r + 8 * h;
+      wrow[m][h] = wbase + row * rb + q * kLaneStep<FMT>;
+      srow[m][h] = sbase + row * sw;
     }
   const __half* xrow[NT];
 #pragma unroll
@@ -255,15 +260,18 @@ COLI_DEV void mx_down_chunk(const MxArgs& A, int e, int o0, int split, int row0,
   const int lane = threadIdx.x & 31, r = lane >> 2, q = lane & 3;
   const size_t rb = mx_row_bytes<FMT>(A.K);
   const int sw = A.K / 128;
+  const size_t e0 = static_cast<size_t>(e) * A.rows_per_expert;
+  const uint8_t* wbase = A.wtab ? A.wtab[e] : A.w + e0 * rb;
+  const uint32_t* sbase = reinterpret_cast<const uint32_t*>(A.stab ? A.stab[e] : A.s + e0 * sw * 4);
   const uint8_t* wrow[2][2];
   const uint32_t* srow[2][2];
 #pragma unroll
   for (int m = 0; m < 2; ++m)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const size_t row = static_cast<size_t>(e) * A.rows_per_expert + o0 + 16 * m + r + 8 * h;
-      wrow[m][h] = A.w + row * rb + q * kLaneStep<FMT>;
-      srow[m][h] = reinterpret_cast<const uint32_t*>(A.s) + row * sw;
+      const size_t row = static_cast<size_t>(o0) + 16 * m + r + 8 * h;  // within the expert
+      wrow[m][h] = wbase + row * rb + q * kLaneStep<FMT>;
+      srow[m][h] = sbase + row * sw;
     }
   const __half* xrow[NT];
 #pragma unroll
@@ -438,6 +446,8 @@ cudaError_t launch_mx_gateup(const FfnWeights& w, const void* x16, const int32_t
   MxArgs A{};
   A.w = static_cast<const uint8_t*>(w.w_gu);
   A.s = static_cast<const uint8_t*>(w.s_gu_u8);
+  A.wtab = w.tab_gu;
+  A.stab = w.tab_sgu;
   A.x = static_cast<const __half*>(x16);
   A.row_token = row_token;
   A.offsets = offsets;
@@ -460,6 +470,8 @@ cudaError_t launch_mx_down(const FfnWeights& w, const void* H16, const int32_t* 
   MxArgs A{};
   A.w = static_cast<const uint8_t*>(w.w_dn);
   A.s = static_cast<const uint8_t*>(w.s_dn_u8);
+  A.wtab = w.tab_dn;
+  A.stab = w.tab_sdn;
   A.x = static_cast<const __half*>(H16);
   A.offsets = offsets;
   A.E = E;
