@@ -69,7 +69,8 @@ def peaks():
 
 def workload_desc(s):
     return (f"{s.name}: T={s.T}, d={s.d}, E={s.E}, k={s.k}, d_ff={s.f}, act={s.act}, "
-            f"experts={s.wdt}" + (", Zipf router bias" if s.bias == "zipf" else ""))
+            f"experts={s.wdt}" + (", Zipf router bias" if s.bias == "zipf" else "")
+            + (f", experts in host memory with {s.slots} HBM slots" if s.slots else ""))
 
 
 def dist_env():
@@ -364,6 +365,39 @@ def roofline(s, path, n_rows, active, avg, ms_fwd, pk, pk_src, config_name):
     return roof
 
 
+def tier_record(s, layer, counts, avg, pk, torch):
+    """Residency tier: bytes each forward reads from HBM slots and from host
+    memory over NVLink-C2C, the FFN's effective host-read rate (host bytes /
+    (FFN time - HBM bytes at the HBM peak)), and a pinned host -> device copy
+    of 1 GiB timed in the same process as the reference rate."""
+    slots, _ = layer.residency()
+    per = 3 * s.f * s.d * 2 if s.wdt == "bf16" else None
+    active = [e for e in range(s.E) if counts[e] > 0]
+    hbm = sum(per for e in active if slots[e] >= 0)
+    host = sum(per for e in active if slots[e] < 0)
+    ffn_s = (avg[2] + avg[3]) / 1e3
+    c2c = host / max(ffn_s - hbm / (pk["hbm_gbs"] * 1e9), 1e-9) / 1e9
+    n = 1 << 30
+    src = torch.empty(n, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(n, dtype=torch.uint8, device="cuda")
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(3):
+        dst.copy_(src, non_blocking=True)
+    b.record()
+    b.synchronize()
+    h2d = 3 * n / (a.elapsed_time(b) / 1e3) / 1e9
+    del src, dst
+    return {"expert_slots": s.slots, "max_promotions": s.promotions,
+            "active_resident": sum(1 for e in active if slots[e] >= 0),
+            "active_streamed": sum(1 for e in active if slots[e] < 0),
+            "bytes_from_hbm": hbm, "bytes_from_host": host,
+            "ffn_host_read_gbs": c2c, "pinned_h2d_copy_gbs": h2d,
+            "frac_of_h2d_copy": c2c / h2d}
+
+
 def measure(s, steps, warmup, world, rank, local, cpu_seconds, with_e2e=True,
             config_name=None):
     """Times `steps` forwards of workload `s` (inputs resident in HBM) and
@@ -377,7 +411,8 @@ def measure(s, steps, warmup, world, rank, local, cpu_seconds, with_e2e=True,
     if rank > 0:  # replicas: same weights, this rank's own tokens
         host["x"] = inputs.random_rows(s.T, s.d, s.act_code, seed=1000 + rank)
     dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in host.items()}
-    layer = moe.MoELayer(s.d, s.f, s.E, s.k, s.T, s.act_code, s.w_code, dev)
+    layer = moe.MoELayer(s.d, s.f, s.E, s.k, s.T, s.act_code, s.w_code, dev,
+                         expert_slots=s.slots, max_promotions=s.promotions)
     x = dev["x"]
     dev = None  # the handle holds its own copy of the weights
     torch.cuda.empty_cache()
@@ -462,6 +497,8 @@ def measure(s, steps, warmup, world, rank, local, cpu_seconds, with_e2e=True,
     roof = roofline(s, path, n_rows, active, avg, elapsed_ms / steps, pk, pk_src,
                     config_name or s.name)
 
+    if s.slots:
+        roof["tier"] = tier_record(s, layer, counts, avg, pk, torch)
     rec = {"workload": workload_desc(s), "path": path, "value": value, "unit": "tokens/s",
            "steps": steps, "warmup": max(3, warmup), "ms_per_step": elapsed_ms / steps,
            "l2": ("L2 flushed between steps" if flush else
@@ -505,7 +542,7 @@ def measure(s, steps, warmup, world, rank, local, cpu_seconds, with_e2e=True,
 # the other workloads measured beside the headline one in a default run:
 # the remaining configurations, then one int4 layer at a prefill batch
 EXTRA = ["mixtral_prefill", "fine_int4", "skewed", "tiny_fp32", "mixtral_prefill_int4",
-         "mixtral_decode_mxfp8", "fine_mxfp4"]
+         "mixtral_decode_mxfp8", "fine_mxfp4", "mixtral_decode_tier"]
 
 
 def sub_steps(s, K: int) -> int:
@@ -513,6 +550,8 @@ def sub_steps(s, K: int) -> int:
     for about 0.3 s of timed work (capped), from a rough cost model."""
     flops = 2.0 * s.T * s.k * 3 * s.d * s.f
     bpw = {"i4g128": 0.53, "mxfp8": 1.03, "mxfp4": 0.53}.get(s.wdt, 2.0)  # bytes per weight
+    if s.slots:
+        bpw *= 8.0  # most experts read over C2C
     est_ms = max(0.02, flops / 1.2e15 * 1e3,
                  3 * s.d * s.f * min(s.E, s.T * s.k) * bpw / 5.0e12 * 1e3)
     return int(max(K, min(400, 300.0 / est_ms)))

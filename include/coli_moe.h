@@ -103,6 +103,21 @@ typedef struct {
                               (with BF16) */
   int32_t has_router_bias; /* 0 or 1 */
   int32_t path;            /* coli_path */
+  /* Expert residency tier (0 = every expert resident in HBM). With
+   * 0 < expert_slots < n_experts, every expert's weights are kept in pinned
+   * host memory (Grace memory on a GB300 node) and expert_slots of them also
+   * in HBM; the decode kernels read a resident expert from HBM and stream any
+   * other straight from host memory over NVLink-C2C. After each forward the
+   * hot set follows the routing history: each expert's score becomes
+   * 0.75 * score + rows routed to it, and up to max_promotions experts of the
+   * top expert_slots by score that are not resident are copied into the
+   * slots of resident experts outside that top set (a bounded look-ahead:
+   * the copies serve the next forward; wth2jhl.online deep dive, sections
+   * 3.1 and 4.2). Placement never changes results (section 8.1): outputs are
+   * bit-identical to a fully resident handle. Decode path only (PREFILL is
+   * COLI_EUNSUPPORTED), bf16 / int4 / MX experts. */
+  int32_t expert_slots;
+  int32_t max_promotions;  /* 0..expert_slots promotions per forward */
 } coli_moe_config;
 
 typedef struct {
@@ -171,6 +186,12 @@ int coli_moe_debug_buffers(const coli_moe* h, const int32_t** topk_idx, const fl
 int coli_moe_copy_debug(const coli_moe* h, int32_t T, int32_t* topk_idx, float* topk_w,
                         float* gap, int32_t* counts, int32_t* offsets, int32_t* row_token,
                         int32_t* assign_row, void* stream);
+
+/* Residency tier state (synchronises `stream`): slot_of[e] (host array of
+ * n_experts) receives the HBM slot holding expert e, or -1 when it is read
+ * from host memory; *promotions the number of experts copied into slots since
+ * create. Either output may be NULL. COLI_EINVAL on a handle without a tier. */
+int coli_moe_residency(const coli_moe* h, int32_t* slot_of, int64_t* promotions, void* stream);
 
 /* Path (coli_path, never AUTO) a forward of T tokens takes on this handle. */
 int coli_moe_path_for(const coli_moe* h, int32_t T);

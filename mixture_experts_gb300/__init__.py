@@ -39,7 +39,7 @@ class ColiError(RuntimeError):
 class coli_moe_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "d_model", "d_ff", "n_experts", "top_k", "max_tokens", "act_dtype", "weight_dtype",
-        "has_router_bias", "path")]
+        "has_router_bias", "path", "expert_slots", "max_promotions")]
 
 
 class coli_moe_weights(ctypes.Structure):
@@ -65,6 +65,7 @@ _SIGS = {
     "coli_moe_debug_buffers": ("I", ["P"] * 8),
     "coli_moe_copy_debug": ("I", ["P", "I", "P", "P", "P", "P", "P", "P", "P", "P"]),
     "coli_moe_path_for": ("I", ["P", "I"]),
+    "coli_moe_residency": ("I", ["P", "P", "P", "P"]),
     "coli_moe_set_timing": ("I", ["P", "I"]),
     "coli_moe_stage_times": ("I", ["P", "P", "I", "P", "P"]),
     "coli_moe_destroy": (None, ["P"]),
@@ -214,6 +215,15 @@ def coli_moe_copy_debug(h, T, topk_idx=None, topk_w=None, gap=None, counts=None,
                                      _ptr(assign_row), _stream(stream))
 
 
+def coli_moe_residency(h, n_experts: int, stream=None):
+    """(status, slot of each expert (-1: read from host memory), promotions
+    since create) of a handle's residency tier; synchronises the stream."""
+    slots = (ctypes.c_int32 * n_experts)()
+    n = ctypes.c_int64()
+    rc = lib().coli_moe_residency(_ptr(h), slots, ctypes.byref(n), _stream(stream))
+    return rc, list(slots), n.value
+
+
 def coli_moe_path_for(h, T) -> int:
     return lib().coli_moe_path_for(_ptr(h), T)
 
@@ -259,10 +269,12 @@ class MoELayer:
     """
 
     def __init__(self, d_model, d_ff, n_experts, top_k, max_tokens, act_dtype, weight_dtype,
-                 weights: dict, path: int = PATH_AUTO, stream=None):
+                 weights: dict, path: int = PATH_AUTO, stream=None, expert_slots: int = 0,
+                 max_promotions: int = 0):
         import torch
         self.cfg = coli_moe_config(d_model, d_ff, n_experts, top_k, max_tokens, act_dtype,
-                                   weight_dtype, int(weights.get("b_router") is not None), path)
+                                   weight_dtype, int(weights.get("b_router") is not None), path,
+                                   expert_slots, max_promotions)
         w = coli_moe_weights(*[_ptr(weights.get(n)) for n in (
             "w_router", "b_router", "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down")])
         rc, h, msg = coli_moe_create(self.cfg, w, stream)
@@ -305,6 +317,12 @@ class MoELayer:
 
     def path_for(self, T: int) -> int:
         return coli_moe_path_for(self.h, T)
+
+    def residency(self, stream=None):
+        """(slot of each expert, -1 = host memory; promotions since create)."""
+        rc, slots, n = coli_moe_residency(self.h, self.cfg.n_experts, stream)
+        _check(rc, "coli_moe_residency")
+        return slots, n
 
     def status(self, stream=None) -> int:
         return coli_moe_device_status(self.h, stream)

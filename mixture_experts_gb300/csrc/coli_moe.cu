@@ -10,6 +10,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "../../include/coli_moe.h"
@@ -129,6 +130,10 @@ struct coli_moe {
   void* x_stage = nullptr;
   void* y_stage = nullptr;
   float* xsum = nullptr;  // int4: 136 * group sums of the gate/up activations, then of H
+  // residency tier (expert_slots > 0)
+  bool tier = false;
+  ResidencyState rs{};
+  std::vector<void*> host_allocs;  // pinned host memory, freed at destroy
   // timing
   bool timing = false;
   TimingSet ring[kTimingRing];
@@ -145,9 +150,22 @@ struct coli_moe {
     if (e == cudaSuccess) allocs.push_back(*p);
     return e;
   }
+  cudaError_t alloc_host(void** host, uint8_t** dev, size_t bytes) {
+    *host = nullptr;
+    *dev = nullptr;
+    if (bytes == 0) return cudaSuccess;
+    cudaError_t e = cudaHostAlloc(host, bytes, cudaHostAllocMapped);
+    if (e != cudaSuccess) return e;
+    host_allocs.push_back(*host);
+    void* d = nullptr;
+    e = cudaHostGetDevicePointer(&d, *host, 0);
+    *dev = static_cast<uint8_t*>(d);
+    return e;
+  }
   ~coli_moe() {
     if (tc) tc_plan_destroy(tc);
     for (void* p : allocs) cudaFree(p);
+    for (void* p : host_allocs) cudaFreeHost(p);
     for (auto& s : ring)
       for (auto& e : s.ev)
         if (e != nullptr) cudaEventDestroy(e);
@@ -188,13 +206,27 @@ int validate_cfg(const coli_moe_config* c, char* err, size_t err_len) {
     return fail(err, err_len, COLI_EUNSUPPORTED, "MX weights run on the decode path only");
   if (c->path < COLI_PATH_AUTO || c->path > COLI_PATH_PREFILL)
     return fail(err, err_len, COLI_EINVAL, "unknown path %d", c->path);
+  if (c->expert_slots < 0 || c->expert_slots > c->n_experts)
+    return fail(err, err_len, COLI_EINVAL, "expert_slots=%d outside [0, n_experts]",
+                c->expert_slots);
+  if (c->expert_slots > 0 && c->expert_slots < c->n_experts) {
+    if (c->max_promotions < 0 || c->max_promotions > c->expert_slots)
+      return fail(err, err_len, COLI_EINVAL, "max_promotions=%d outside [0, expert_slots]",
+                  c->max_promotions);
+    if (c->weight_dtype == COLI_F32)
+      return fail(err, err_len, COLI_EUNSUPPORTED,
+                  "the residency tier serves bf16, int4 and MX experts");
+    if (c->path == COLI_PATH_PREFILL)
+      return fail(err, err_len, COLI_EUNSUPPORTED,
+                  "the residency tier runs on the decode path only");
+  }
   return COLI_OK;
 }
 
 int pick_path(const coli_moe* h, int T) {
   const auto& c = h->cfg;
   if (c.weight_dtype == COLI_F32) return COLI_PATH_DECODE;  // CUDA-core fp32 path
-  if (h->tc == nullptr) return COLI_PATH_DECODE;
+  if (h->tier || h->tc == nullptr) return COLI_PATH_DECODE;
   if (c.path != COLI_PATH_AUTO) return c.path;
   return static_cast<long>(T) * c.top_k <= 64L * c.n_experts ? COLI_PATH_DECODE
                                                              : COLI_PATH_PREFILL;
@@ -397,16 +429,19 @@ int coli_moe_create(const coli_moe_config* cfg, const coli_moe_weights* wts, voi
   }
   void *wgu = nullptr, *wdn = nullptr, *sgu = nullptr, *sdn = nullptr;
   const int hsz = cfg->weight_dtype == COLI_F32 ? 4 : 2;
+  // residency tier: the expert weights go to pinned host memory instead
+  const bool tier = cfg->expert_slots > 0 && cfg->expert_slots < E;
+  const int S = tier ? cfg->expert_slots : 0, P = tier ? cfg->max_promotions : 0;
   struct {
     void** p;
     size_t n;
   } plan[] = {
       {&h->w_router, wr_bytes},
       {reinterpret_cast<void**>(&h->b_router), cfg->has_router_bias ? E * sizeof(float) : 0},
-      {&wgu, gu_bytes},
-      {&wdn, dn_bytes},
-      {&sgu, sgu_bytes},
-      {&sdn, sdn_bytes},
+      {&wgu, tier ? 0 : gu_bytes},
+      {&wdn, tier ? 0 : dn_bytes},
+      {&sgu, tier ? 0 : sgu_bytes},
+      {&sdn, tier ? 0 : sdn_bytes},
       {reinterpret_cast<void**>(&h->topk_idx), Na * sizeof(int32_t)},
       {reinterpret_cast<void**>(&h->topk_w), Na * sizeof(float)},
       {reinterpret_cast<void**>(&h->gap), Tm * sizeof(float)},
@@ -427,6 +462,45 @@ int coli_moe_create(const coli_moe_config* cfg, const coli_moe_weights* wts, voi
   };
   for (auto& a : plan)
     if ((e = h->alloc(a.p, a.n)) != cudaSuccess) return bail(COLI_ENOMEM, "cudaMalloc", e);
+  if (tier) {
+    ResidencyState& R = h->rs;
+    void* host[4];
+    if ((e = h->alloc_host(&host[0], &R.host_gu, gu_bytes)) != cudaSuccess ||
+        (e = h->alloc_host(&host[1], &R.host_dn, dn_bytes)) != cudaSuccess ||
+        (e = h->alloc_host(&host[2], &R.host_sgu, sgu_bytes)) != cudaSuccess ||
+        (e = h->alloc_host(&host[3], &R.host_sdn, sdn_bytes)) != cudaSuccess)
+      return bail(COLI_ENOMEM, "pinned host memory for the experts", e);
+    wgu = R.host_gu;
+    wdn = R.host_dn;
+    sgu = R.host_sgu;
+    sdn = R.host_sdn;
+    R.gu_bytes = gu_bytes / E;
+    R.dn_bytes = dn_bytes / E;
+    R.sgu_bytes = sgu_bytes / E;
+    R.sdn_bytes = sdn_bytes / E;
+    struct {
+      void** p;
+      size_t n;
+    } tp[] = {
+        {reinterpret_cast<void**>(&R.slot_gu), S * R.gu_bytes},
+        {reinterpret_cast<void**>(&R.slot_dn), S * R.dn_bytes},
+        {reinterpret_cast<void**>(&R.slot_sgu), S * R.sgu_bytes},
+        {reinterpret_cast<void**>(&R.slot_sdn), S * R.sdn_bytes},
+        {reinterpret_cast<void**>(&R.tab_gu), E * sizeof(void*)},
+        {reinterpret_cast<void**>(&R.tab_dn), E * sizeof(void*)},
+        {reinterpret_cast<void**>(&R.tab_sgu), E * sizeof(void*)},
+        {reinterpret_cast<void**>(&R.tab_sdn), E * sizeof(void*)},
+        {reinterpret_cast<void**>(&R.score), E * sizeof(float)},
+        {reinterpret_cast<void**>(&R.slot_of), E * sizeof(int32_t)},
+        {reinterpret_cast<void**>(&R.expert_in), S * sizeof(int32_t)},
+        {reinterpret_cast<void**>(&R.copy_list), 2 * (P > 0 ? P : 1) * sizeof(int32_t)},
+        {reinterpret_cast<void**>(&R.n_copy), sizeof(int32_t)},
+        {reinterpret_cast<void**>(&R.promotions), sizeof(int32_t)},
+    };
+    for (auto& a : tp)
+      if ((e = h->alloc(a.p, a.n)) != cudaSuccess) return bail(COLI_ENOMEM, "cudaMalloc", e);
+    h->tier = true;
+  }
   if ((e = cudaMemcpyAsync(h->w_router, wts->w_router, wr_bytes, cudaMemcpyDefault, st)) !=
       cudaSuccess)
     return bail(COLI_ECUDA, "copy router weights", e);
@@ -442,11 +516,53 @@ int coli_moe_create(const coli_moe_config* cfg, const coli_moe_weights* wts, voi
   h->w.wdt = cfg->weight_dtype;
   h->w.w_gu = wgu;
   h->w.w_dn = wdn;
+  if (tier) {
+    // experts 0..S-1 start in the slots; the tables point every other expert
+    // at its host copy
+    ResidencyState& R = h->rs;
+    const std::pair<uint8_t*, uint8_t*> part[4] = {{R.slot_gu, R.host_gu}, {R.slot_dn, R.host_dn},
+                                                   {R.slot_sgu, R.host_sgu}, {R.slot_sdn, R.host_sdn}};
+    const size_t per[4] = {R.gu_bytes, R.dn_bytes, R.sgu_bytes, R.sdn_bytes};
+    std::vector<const uint8_t*> tab[4];
+    for (int i = 0; i < 4; ++i) {
+      if (per[i] > 0 &&
+          (e = cudaMemcpyAsync(part[i].first, part[i].second, S * per[i], cudaMemcpyDefault,
+                               st)) != cudaSuccess)
+        return bail(COLI_ECUDA, "initial expert slots", e);
+      // expert x < S sits in slot x, the others are read from their host copy
+      tab[i].resize(E);
+      for (int x = 0; x < E; ++x)
+        tab[i][x] = per[i] == 0 ? nullptr
+                                : (x < S ? part[i].first : part[i].second) +
+                                      static_cast<size_t>(x) * per[i];
+    }
+    std::vector<int32_t> slot_of(E), expert_in(S);
+    for (int x = 0; x < E; ++x) slot_of[x] = x < S ? x : -1;
+    for (int x = 0; x < S; ++x) expert_in[x] = x;
+    const uint8_t** dst[4] = {R.tab_gu, R.tab_dn, R.tab_sgu, R.tab_sdn};
+    for (int i = 0; i < 4; ++i)
+      if ((e = cudaMemcpyAsync(dst[i], tab[i].data(), E * sizeof(void*), cudaMemcpyHostToDevice,
+                               st)) != cudaSuccess)
+        return bail(COLI_ECUDA, "residency tables", e);
+    if ((e = cudaMemcpyAsync(R.slot_of, slot_of.data(), E * sizeof(int32_t),
+                             cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(R.expert_in, expert_in.data(), S * sizeof(int32_t),
+                             cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+        (e = cudaMemsetAsync(R.score, 0, E * sizeof(float), st)) != cudaSuccess ||
+        (e = cudaMemsetAsync(R.promotions, 0, sizeof(int32_t), st)) != cudaSuccess ||
+        (e = cudaMemsetAsync(R.n_copy, 0, sizeof(int32_t), st)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(st)) != cudaSuccess)  // the host tables above go out of scope
+      return bail(COLI_ECUDA, "residency state", e);
+    h->w.tab_gu = R.tab_gu;
+    h->w.tab_dn = R.tab_dn;
+    h->w.tab_sgu = R.sgu_bytes ? R.tab_sgu : nullptr;
+    h->w.tab_sdn = R.sdn_bytes ? R.tab_sdn : nullptr;
+  }
   h->w.s_gu_u8 = mx ? static_cast<const uint8_t*>(sgu) : nullptr;
   h->w.s_dn_u8 = mx ? static_cast<const uint8_t*>(sdn) : nullptr;
   h->w.s_gu = static_cast<const __nv_bfloat16*>(sgu);
   h->w.s_dn = static_cast<const __nv_bfloat16*>(sdn);
-  if ((cfg->weight_dtype == COLI_BF16 || i4) && tc_supported(d, f)) {
+  if ((cfg->weight_dtype == COLI_BF16 || i4) && !tier && tc_supported(d, f)) {
     if ((e = tc_plan_create(&h->tc, cfg->weight_dtype, wgu, wdn, h->w.s_gu, h->w.s_dn, E, d, f,
                             static_cast<int>(Na), h->x_perm, h->H)) != cudaSuccess)
       return bail(COLI_ECUDA, "tensor-core plan", e);
@@ -502,6 +618,12 @@ int coli_moe_forward(coli_moe* h, const void* x, int32_t T, void* y, void* strea
                             h->topk_w, T, k, d, c.act_dtype, y, st, status));
   }
   launches += 1;
+  if (h->tier && c.max_promotions > 0) {
+    // the hot set follows this forward's routing; copies serve the next one
+    CUDA_TRY(launch_residency_update(h->counts, E, c.expert_slots, c.max_promotions, h->rs,
+                                     h->num_sms * 4, st));
+    launches += 2;
+  }
   timing_mark(h, ts, 5, st);
   if (ts) {
     ts->launches = launches;
@@ -568,6 +690,24 @@ int coli_moe_copy_debug(const coli_moe* h, int32_t T, int32_t* topk_idx, float* 
   for (auto& c : cp)
     if (c.dst != nullptr && c.n > 0)
       CUDA_TRY(cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToDevice, st));
+  return COLI_OK;
+}
+
+int coli_moe_residency(const coli_moe* h, int32_t* slot_of, int64_t* promotions, void* stream) {
+  char* err = nullptr;
+  size_t err_len = 0;
+  if (h == nullptr) return fail(err, err_len, COLI_EINVAL, "handle is NULL");
+  if (!h->tier) return fail(err, err_len, COLI_EINVAL, "the handle has no residency tier");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CUDA_TRY(cudaStreamSynchronize(st));
+  if (slot_of)
+    CUDA_TRY(cudaMemcpy(slot_of, h->rs.slot_of, h->cfg.n_experts * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost));
+  if (promotions) {
+    int32_t p = 0;
+    CUDA_TRY(cudaMemcpy(&p, h->rs.promotions, sizeof p, cudaMemcpyDeviceToHost));
+    *promotions = p;
+  }
   return COLI_OK;
 }
 

@@ -67,6 +67,8 @@ class MoEShape:
     wdt: str = "bf16"      # "f32" | "bf16" | "i4g128" | "mxfp8" | "mxfp4"
     bias: str = "none"     # "none" | "zipf" | "hot0"
     alpha: float = SKEWED_ALPHA
+    slots: int = 0         # handle option: experts kept in HBM (0 = all); the rest in host memory
+    promotions: int = 0    # handle option: hot-set promotions per forward
 
     @property
     def act_code(self) -> int:
@@ -102,6 +104,10 @@ CONFIGS = {
     "mixtral_decode_mxfp8": MoEShape("mixtral_decode_mxfp8", T=32, d=4096, E=8, k=2, f=14336,
                                      wdt="mxfp8"),
     "fine_mxfp4": MoEShape("fine_mxfp4", T=256, d=6144, E=256, k=8, f=2048, wdt="mxfp4"),
+    # the decode layer with its experts in host memory and 2 of 8 in HBM:
+    # 6 active experts stream over NVLink-C2C every forward
+    "mixtral_decode_tier": MoEShape("mixtral_decode_tier", T=32, d=4096, E=8, k=2, f=14336,
+                                    slots=2, promotions=0),
 }
 
 

@@ -59,6 +59,24 @@ def test_create_rejects_mx_shapes_and_prefill(lib, wdt):
     assert rc == moe.COLI_EINVAL
 
 
+def test_create_rejects_bad_residency_tiers(lib):
+    base = dict(d=256, f=512, E=8, k=2, T=16)
+
+    def cfg(act, wdt, path, slots, promo):
+        return moe.coli_moe_config(base["d"], base["f"], base["E"], base["k"], base["T"], act,
+                                   wdt, 0, path, slots, promo)
+    for c, code, word in [
+            (cfg(moe.BF16, moe.BF16, 0, 9, 0), moe.COLI_EINVAL, "expert_slots"),
+            (cfg(moe.BF16, moe.BF16, 0, -1, 0), moe.COLI_EINVAL, "expert_slots"),
+            (cfg(moe.BF16, moe.BF16, 0, 4, 5), moe.COLI_EINVAL, "max_promotions"),
+            (cfg(moe.F32, moe.F32, 0, 4, 1), moe.COLI_EUNSUPPORTED, "bf16"),
+            (cfg(moe.BF16, moe.I4G128, moe.PATH_PREFILL, 4, 1), moe.COLI_EUNSUPPORTED,
+             "decode")]:
+        rc, _, msg = moe.coli_moe_create(c, moe.coli_moe_weights(), stream=0)
+        assert rc == code and word in msg, (rc, msg)
+    assert moe.coli_moe_residency(None, 8)[0] == moe.COLI_EINVAL
+
+
 def test_create_rejects_missing_weights(lib):
     cfg = moe.coli_moe_config(256, 512, 8, 2, 16, moe.BF16, moe.BF16, 0, 0)
     rc, _, msg = moe.coli_moe_create(cfg, moe.coli_moe_weights(), stream=0)

@@ -20,7 +20,7 @@ C_PROGRAM = r"""
 int main(void) {
   char err[256] = {0};
   coli_moe* h = NULL;
-  coli_moe_config cfg = {256, 512, 8, 2, 16, COLI_BF16, COLI_BF16, 0, COLI_PATH_AUTO};
+  coli_moe_config cfg = {256, 512, 8, 2, 16, COLI_BF16, COLI_BF16, 0, COLI_PATH_AUTO, 0, 0};
   coli_moe_weights w;
   memset(&w, 0, sizeof w);
   if (strstr(coli_version(), "sm_103a") == NULL) return 10;
@@ -34,6 +34,10 @@ int main(void) {
                       NULL) != COLI_EINVAL)
     return 15;
   if (coli_permute_scratch_bytes(4, 2, 8) != 0) return 16;
+  /* residency query on no handle; a tier with more slots than experts */
+  if (coli_moe_residency(NULL, NULL, NULL, NULL) != COLI_EINVAL) return 17;
+  cfg.expert_slots = 9;
+  if (coli_moe_create(&cfg, &w, NULL, &h, err, sizeof err) != COLI_EINVAL) return 18;
   printf("%s\n", err);
   return 0;
 }

@@ -8,7 +8,7 @@ import torch
 import mixture_experts_gb300 as moe
 import oracle
 from mixture_experts_gb300 import inputs
-from parity import (TOL, check_dispatch, check_routing, cuda_layer, host_dict, make_handle,
+from parity import (TOL, check_layer, check_routing, cuda_layer, host_dict, make_handle,
                     oracle_routing, rel_err, y_to_f64)
 
 pytestmark = pytest.mark.gpu
@@ -52,27 +52,6 @@ def run_layer(s, lay, path=moe.PATH_AUTO):
     torch.cuda.synchronize()
     assert layer.status() == moe.COLI_OK
     return layer, y, host_dict(dbg)
-
-
-def check_layer(s, lay, y, dbg, threads=1, sample=None):
-    """Routing and dispatch of every token against the oracle, then the output
-    of every token that is not a near-tie (or of `sample` seeded tokens),
-    element by element."""
-    idx, w, gap, inner = oracle_routing(s, lay)
-    near = check_routing(dbg["topk_idx"], dbg["topk_w"], idx, w, gap, inner)
-    check_dispatch(dbg, idx, near, s.E)
-    assert np.allclose(dbg["gap"][~near], gap[~near], rtol=0, atol=1e-5)
-    tokens = np.nonzero(~near)[0].astype(np.int32)
-    if sample is not None and sample < len(tokens):
-        pick = np.random.default_rng(0).choice(len(tokens), sample, replace=False)
-        tokens = np.sort(np.concatenate([tokens[pick], tokens[[0, -1]]]))
-        tokens = np.unique(tokens).astype(np.int32)
-    ref = oracle.moe_forward(lay, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f, tokens=tokens,
-                             threads=threads)
-    got = y_to_f64(y)[tokens]
-    err = rel_err(got, ref["y_f64"])
-    assert err <= TOL[s.wdt], f"{s.name}: max|err|/max|ref| = {err:.3e}"
-    return err, int(near.sum())
 
 
 @pytest.mark.parametrize("name", list(SMALL))
