@@ -414,6 +414,270 @@ __global__ void __launch_bounds__(Shape<I4>::kThreads, 1)
   }
 }
 
+// ---- CTA-pair kernel (bf16 weights) ------------------------------------------------
+// A pair of CTAs (a cluster of two, one per SM) computes a 256-row x 256-column
+// tile with cta_group::2 MMAs issued by the first CTA: each CTA loads its own
+// 128 activation rows and half (128 rows) of the weight tile into its shared
+// memory, and the tensor cores of the pair read both halves, so a CTA moves
+// 32 KiB per 64-deep stage instead of 48 KiB for the same MMA work. Each
+// CTA's tensor memory receives its 128 rows of the accumulator and its own
+// four epilogue warps drain them. The first CTA's barriers count the pair's
+// TMA bytes and both CTAs' epilogue arrivals; its MMA commits arrive on the
+// matching barriers of both CTAs.
+constexpr int PAIR_STAGES = 6;
+constexpr int BH_BYTES = (BN / 2) * BK * 2;  // 16 KiB: a CTA's half of the weight tile
+constexpr uint32_t kIdescPair = idesc_bf16(2 * BM, BN);
+
+struct __align__(8) CtrlPair {
+  uint64_t full[PAIR_STAGES], empty[PAIR_STAGES], tfull[2], tempty[2];
+  uint32_t tmem_base;
+  int abort;
+  int tile_off[kMaxE + 1];
+  int row_off[kMaxE + 1];
+};
+
+// 16 KiB of headroom after the weight stages: every operand read of the MMAs
+// stays inside this CTA's allocation whatever the stage.
+constexpr int kPairGuard = 16384;
+constexpr size_t kPairSmem =
+    1024 + PAIR_STAGES * (A_BYTES + BH_BYTES) + kPairGuard + sizeof(CtrlPair);
+
+// Tile t of the pair grid: expert, 256-column tile, 256-row tile.
+COLI_DEV Tile decode_pair_tile(const CtrlPair& C, int E, int t) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (C.tile_off[mid] <= t) lo = mid;
+    else hi = mid;
+  }
+  const int rows = C.row_off[lo + 1] - C.row_off[lo];
+  const int mts = (rows + 2 * BM - 1) / (2 * BM);
+  const int local = t - C.tile_off[lo];
+  return Tile{lo, local / mts, local % mts};
+}
+
+template <int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    k_tc_gemm_pair(const __grid_constant__ CUtensorMap map_a,
+                   const __grid_constant__ CUtensorMap map_b, const int32_t* __restrict__ offsets,
+                   int E, int K, int N, void* __restrict__ out, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sa = smem_u32(base);
+  const uint32_t sb = sa + PAIR_STAGES * A_BYTES;
+  CtrlPair& C =
+      *reinterpret_cast<CtrlPair*>(base + PAIR_STAGES * (A_BYTES + BH_BYTES) + kPairGuard);
+  volatile int* abort = &C.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool first = rank == 0;
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+  const uint64_t deadline = global_timer_ns() + kWaitTimeoutNs;
+  const int n_tiles_n = (N + BN - 1) / BN;
+  const int kblocks = K / BK;
+
+  if (warp == 0) {
+    int mts[kMaxE / 32], sum = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {
+      const int e = lane * (kMaxE / 32) + i;
+      int m = 0;
+      if (e < E) {
+        const int r0 = offsets[e], r1 = offsets[e + 1];
+        C.row_off[e] = r0;
+        if (e == E - 1) C.row_off[E] = r1;
+        m = ((r1 - r0 + 2 * BM - 1) / (2 * BM)) * n_tiles_n;
+      }
+      mts[i] = m;
+      sum += m;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {
+      const int e = lane * (kMaxE / 32) + i;
+      if (e < E) C.tile_off[e] = run;
+      run += mts[i];
+    }
+    if (lane == 31) C.tile_off[E] = incl;
+    if (lane == 0) {
+      for (int st = 0; st < PAIR_STAGES; ++st) {
+        mbar_init(smem_u32(&C.full[st]), 1);
+        mbar_init(smem_u32(&C.empty[st]), 1);
+      }
+      for (int a = 0; a < 2; ++a) {
+        mbar_init(smem_u32(&C.tfull[a]), 1);
+        mbar_init(smem_u32(&C.tempty[a]), 8);  // four epilogue warps in each CTA
+      }
+      C.abort = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+  } else if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&C.tmem_base), TMEM_COLS);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before anything arrives on them
+  tc_fence_after();
+  const uint32_t tmem = C.tmem_base;
+  const int total = C.tile_off[E];
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer (both CTAs): own rows, own half of B
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = pair; t < total && !*abort; t += n_pairs) {
+        const Tile tl = decode_pair_tile(C, E, t);
+        const int a_row = C.row_off[tl.e] + tl.mt * 2 * BM + static_cast<int>(rank) * BM;
+        const int b_row = tl.e * N + tl.nt * BN + static_cast<int>(rank) * (BN / 2);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!wait_bar_cluster(smem_u32(&C.empty[stage]), phase ^ 1u, deadline, abort)) break;
+          const uint32_t fb = smem_u32(&C.full[stage]);
+          if (first) mbar_arrive_expect_tx(fb, 2 * (A_BYTES + BH_BYTES));
+          const uint32_t fb0 = map_shared(fb, 0);
+          tma_load_2d_pair(sa + stage * A_BYTES, &map_a, fb0, kb * BK, a_row);
+          tma_load_2d_pair(sb + stage * BH_BYTES, &map_b, fb0, kb * BK, b_row);
+          if (++stage == PAIR_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && first) {  // ---- MMA issuer (first CTA of the pair)
+      int stage = 0, local = 0;
+      uint32_t phase = 0;
+      for (int t = pair; t < total && !*abort; t += n_pairs, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!wait_bar_cluster(smem_u32(&C.tempty[acc]), acc_phase ^ 1u, deadline, abort)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!wait_bar_cluster(smem_u32(&C.full[stage]), phase, deadline, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = sa + stage * A_BYTES, b0 = sb + stage * BH_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_ss_pair(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), kIdescPair,
+                         (kb | k) != 0 ? 1u : 0u);
+          umma_commit_pair(smem_u32(&C.empty[stage]));
+          if (++stage == PAIR_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(smem_u32(&C.tfull[acc]));
+      }
+    }
+  } else {  // ---- epilogue (both CTAs): warps 2..5, this CTA's 128 rows
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;
+    int local = 0;
+    for (int t = pair; t < total && !*abort; t += n_pairs, ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!__all_sync(0xffffffffu,
+                      wait_bar_cluster(smem_u32(&C.tfull[acc]), acc_phase, deadline, abort)))
+        break;
+      tc_fence_after();
+      const Tile tl = decode_pair_tile(C, E, t);
+      const int row = C.row_off[tl.e] + tl.mt * 2 * BM + static_cast<int>(rank) * BM + r;
+      const bool valid = row < C.row_off[tl.e + 1];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(qw * 32) << 16) + acc * BN;
+      if constexpr (EPI == 0) {
+        const int F = N / 2;
+        __nv_bfloat16* H = static_cast<__nv_bfloat16*>(out);
+#pragma unroll 1
+        for (int ci = 0; ci < 4; ++ci) {
+          const int c = (ci & 1) + (ci >> 1) * 4;
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c * 32, g);
+          tmem_ld32(taddr + (c + 2) * 32, u);
+          const int feat = tl.nt * 128 + (c & 1) * 32 + (c >> 2) * 64;
+          if (valid && feat < F) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float a0 = __uint_as_float(g[2 * j]), a1 = __uint_as_float(g[2 * j + 1]);
+              const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
+              packed[j] = pack_bf16x2(a0 / (1.f + expf(-a0)) * u0, a1 / (1.f + expf(-a1)) * u1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(H + static_cast<size_t>(row) * F + feat);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                  packed[4 * v + 3]);
+          }
+        }
+      } else if constexpr (EPI == 1) {
+        float* Y = static_cast<float*>(out);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c * 32, v);
+          const int col = tl.nt * BN + c * 32;
+          if (valid && col < N) {
+            uint4* dst = reinterpret_cast<uint4*>(Y + static_cast<size_t>(row) * N + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        }
+      } else {
+        __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(out);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c * 32, v);
+          const int col = tl.nt * BN + c * 32;
+          if (valid && col < N) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            uint4* dst = reinterpret_cast<uint4*>(Y + static_cast<size_t>(row) * N + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_shared(smem_u32(&C.tempty[acc]), 0));
+    }
+  }
+
+  __syncthreads();
+  if (*abort) {
+    if (threadIdx.x == 0) {
+      latch_error(status, kErrTimeout);
+      const uint64_t t0 = global_timer_ns();  // let copies in flight land
+      while (global_timer_ns() - t0 < 1000000ull) {
+      }
+    }
+    __syncthreads();
+  }
+  cluster_sync();  // neither CTA frees tensor memory or exits while the pair still works
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, TMEM_COLS);
+  }
+}
+
 // 2-D bf16 [rows][cols] row-major, box [box_rows][64], 128-byte swizzle.
 cudaError_t make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, int box_rows) {
   return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, rows, cols, BK, box_rows,
@@ -453,6 +717,7 @@ cudaError_t encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_byte
 struct TcPlan {
   CUtensorMap map_wgu, map_wdn, map_xperm, map_h;
   bool i4;
+  bool pair;  // bf16 weights: CTA-pair kernel with half-height weight maps
   const __nv_bfloat16 *s_gu, *s_dn;  // int4 scales [rows][K/128]
   int E, d, f, grid;
 };
@@ -498,11 +763,19 @@ cudaError_t tc_plan_create(TcPlan** plan, int wdt, const void* w_gu, const void*
     if (e == cudaSuccess) e = set_smem<1, true>();
     if (e == cudaSuccess) e = set_smem<2, true>();
   } else {
-    e = make_map(&p->map_wgu, w_gu, static_cast<uint64_t>(E) * 2 * f, d, BN);
-    if (e == cudaSuccess) e = make_map(&p->map_wdn, w_dn, static_cast<uint64_t>(E) * d, f, BN);
+    // each CTA of a pair loads 128 of the 256 weight rows of a tile
+    p->pair = sms >= 2;
+    const int box = p->pair ? BN / 2 : BN;
+    e = make_map(&p->map_wgu, w_gu, static_cast<uint64_t>(E) * 2 * f, d, box);
+    if (e == cudaSuccess) e = make_map(&p->map_wdn, w_dn, static_cast<uint64_t>(E) * d, f, box);
     if (e == cudaSuccess) e = set_smem<0, false>();
     if (e == cudaSuccess) e = set_smem<1, false>();
     if (e == cudaSuccess) e = set_smem<2, false>();
+    for (auto fn : {k_tc_gemm_pair<0>, k_tc_gemm_pair<1>, k_tc_gemm_pair<2>})
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kPairSmem));
+    if (p->pair) p->grid = sms & ~1;  // whole pairs
   }
   if (e == cudaSuccess) e = make_map(&p->map_xperm, x_perm, static_cast<uint64_t>(max_rows), d, BM);
   if (e == cudaSuccess) e = make_map(&p->map_h, H, static_cast<uint64_t>(max_rows), f, BM);
@@ -520,7 +793,10 @@ template <int EPI>
 static void launch(const TcPlan* p, const CUtensorMap& map_a, const CUtensorMap& map_b,
                    const int32_t* offsets, int K, int N, void* out, I4Args q4, cudaStream_t st,
                    int* status) {
-  if (p->i4)
+  if (p->pair)
+    k_tc_gemm_pair<EPI><<<p->grid, 192, kPairSmem, st>>>(map_a, map_b, offsets, p->E, K, N, out,
+                                                         status);
+  else if (p->i4)
     k_tc_gemm<EPI, true><<<p->grid, Shape<true>::kThreads, smem_bytes<true>(), st>>>(
         map_a, map_b, offsets, p->E, K, N, out, q4, status);
   else
