@@ -294,6 +294,9 @@ def traffic_record(config: str, kind: str):
 
 
 # ---------------------------------------------------------------- GPU leg
+QNAME = {"i4g128": "int4", "mxfp8": "E4M3", "mxfp4": "E2M1"}  # quantised expert formats
+
+
 def roofline(s, path, n_rows, active, avg, ms_fwd, pk, pk_src, config_name):
     """Dominant kernel's roofline (gate/up projection: the decode weight
     stream or the prefill grouped GEMM) plus whole-layer figures."""
@@ -338,9 +341,9 @@ def roofline(s, path, n_rows, active, avg, ms_fwd, pk, pk_src, config_name):
                 "frac": achieved / sust, "frac_burst": achieved / burst,
                 "frac_sustained": achieved / sust,
                 "traffic": traffic_record(config_name, "tc"),
-                "kernel": ("k_tc_gemm<int4> (gate/up grouped GEMM, int4 weights dequantised "
-                           "to bf16 in shared memory, + SwiGLU)" if s.wdt == "i4g128" else
-                           "k_tc_gemm (gate/up grouped GEMM + SwiGLU)"),
+                "kernel": (f"k_tcq_gemm<{QNAME[s.wdt]}> (gate/up grouped GEMM, weights "
+                           "dequantised into tensor memory, + SwiGLU)" if s.wdt in QNAME else
+                           "k_tc_gemm_pair (gate/up grouped GEMM on CTA pairs + SwiGLU)"),
                 "algorithmic_flops_per_launch": flops,
                 "unit_work": f"2 x {n_rows} rows x d={s.d} x 2f={2 * s.f} FLOP",
                 "peak_source": f"{pk_src} bf16_tflops_sustained (burst {burst})"}
@@ -357,11 +360,13 @@ def roofline(s, path, n_rows, active, avg, ms_fwd, pk, pk_src, config_name):
     # bf16/int4 experts reads token rows of x directly and writes no x_perm
     asz = 4 if s.act == "f32" else 2
     xperm = 0 if (path == "decode" and s.wdt != "f32") else 2 * n_rows * s.d * asz
-    if s.wdt in ("mxfp8", "mxfp4"):
+    if path == "decode" and s.wdt in ("mxfp8", "mxfp4"):
         xperm = 2 * s.T * s.d * 2  # the fp16 copy of the token rows
+    # the prefill path writes y_perm in bf16 for bf16 activations
+    ysz = 2 if (path == "prefill" and s.act == "bf16") else 4
     roof["overhead_bytes"] = {
         "x_perm": xperm, "H": 2 * n_rows * s.f * (4 if s.wdt == "f32" else 2),
-        "y_perm": 2 * n_rows * s.d * 4}
+        "y_perm": 2 * n_rows * s.d * ysz}
     return roof
 
 
@@ -540,9 +545,9 @@ def measure(s, steps, warmup, world, rank, local, cpu_seconds, with_e2e=True,
 
 
 # the other workloads measured beside the headline one in a default run:
-# the remaining configurations, then one int4 layer at a prefill batch
+# the remaining configurations, then the quantised-expert and residency layers
 EXTRA = ["mixtral_prefill", "fine_int4", "skewed", "tiny_fp32", "mixtral_prefill_int4",
-         "mixtral_decode_mxfp8", "fine_mxfp4", "mixtral_decode_tier"]
+         "mixtral_prefill_mxfp8", "mixtral_decode_mxfp8", "fine_mxfp4", "mixtral_decode_tier"]
 
 
 def sub_steps(s, K: int) -> int:

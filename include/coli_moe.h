@@ -68,9 +68,11 @@ typedef enum {
  *   COLI_MXFP4:  OCP Microscaling E2M1 nibbles [..][cols/2] (low nibble = even
  *                index), E8M0 scale bytes [..][cols/32].
  * MX formats are the block-scaled low-precision weights of the model families
- * in the wth2jhl.online deep dive's table (MXFP4, FP8); they run on the
- * decode path with fp16 activations (values beyond the fp16 range are
- * saturated and latch COLI_EDEVICE). */
+ * in the wth2jhl.online deep dive's table (MXFP4, FP8). The decode path runs
+ * them with fp16 activations (values beyond the fp16 range are saturated and
+ * latch COLI_EDEVICE); the prefill path dequantises each weight exactly to a
+ * bf16 tensor-core operand (an E4M3/E2M1 value times a power of two; a
+ * product beyond bf16's range rounds to it, NaN codes and scales give NaN). */
 typedef enum {
   COLI_F32 = 0,
   COLI_BF16 = 1,
@@ -83,13 +85,14 @@ typedef enum {
  * (T*k/E) is at most 64, else PREFILL. DECODE streams each active expert's
  * weights once (tensor-core MMA fed straight from HBM); PREFILL is the
  * TMA + tcgen05/TMEM grouped GEMM. Both give the same routing and the same
- * outputs within rounding. F32 layers always use the CUDA-core path; MX
- * layers always use DECODE (PREFILL is COLI_EUNSUPPORTED for them).
+ * outputs within rounding. F32 layers always use the CUDA-core path.
  * int4 experts run on both: DECODE applies each group's scale to the exact
  * sum of q*x in fp32 (w = q*s exactly); PREFILL dequantises each weight to a
  * bf16 tensor-core operand, q*s rounded once to nearest even (q*s can need 11
  * significant bits, bf16 holds 8: a relative change of at most 2^-9 per
- * weight). */
+ * weight). A layer has no PREFILL form (and runs DECODE whatever `path`
+ * asks) with 4-bit experts (int4, MXFP4) when d_model or d_ff is 128, or
+ * with the residency tier. */
 typedef enum { COLI_PATH_AUTO = 0, COLI_PATH_DECODE = 1, COLI_PATH_PREFILL = 2 } coli_path;
 
 typedef struct {

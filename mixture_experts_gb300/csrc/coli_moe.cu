@@ -201,9 +201,6 @@ int validate_cfg(const coli_moe_config* c, char* err, size_t err_len) {
   if ((c->weight_dtype == COLI_MXFP8 || c->weight_dtype == COLI_MXFP4) &&
       (c->d_model % 128 || c->d_ff % 128))
     return fail(err, err_len, COLI_EINVAL, "MX weights need d_model and d_ff multiples of 128");
-  if ((c->weight_dtype == COLI_MXFP8 || c->weight_dtype == COLI_MXFP4) &&
-      c->path == COLI_PATH_PREFILL)
-    return fail(err, err_len, COLI_EUNSUPPORTED, "MX weights run on the decode path only");
   if (c->path < COLI_PATH_AUTO || c->path > COLI_PATH_PREFILL)
     return fail(err, err_len, COLI_EINVAL, "unknown path %d", c->path);
   if (c->expert_slots < 0 || c->expert_slots > c->n_experts)
@@ -562,9 +559,24 @@ int coli_moe_create(const coli_moe_config* cfg, const coli_moe_weights* wts, voi
   h->w.s_dn_u8 = mx ? static_cast<const uint8_t*>(sdn) : nullptr;
   h->w.s_gu = static_cast<const __nv_bfloat16*>(sgu);
   h->w.s_dn = static_cast<const __nv_bfloat16*>(sdn);
-  if ((cfg->weight_dtype == COLI_BF16 || i4) && !tier && tc_supported(d, f)) {
-    if ((e = tc_plan_create(&h->tc, cfg->weight_dtype, wgu, wdn, h->w.s_gu, h->w.s_dn, E, d, f,
-                            static_cast<int>(Na), h->x_perm, h->H)) != cudaSuccess)
+  if (cfg->weight_dtype != COLI_F32 && !tier && tc_supported(cfg->weight_dtype, d, f)) {
+    // MX weights outside the converters' fast range take their exact path
+    int general = 0;
+    if (mx) {
+      int* flag = nullptr;
+      if ((e = h->alloc(reinterpret_cast<void**>(&flag), sizeof(int))) != cudaSuccess ||
+          (e = cudaMemsetAsync(flag, 0, sizeof(int), st)) != cudaSuccess ||
+          (e = launch_mx_scan(wgu, gu_bytes, sgu, sgu_bytes, cfg->weight_dtype, flag, st)) !=
+              cudaSuccess ||
+          (e = launch_mx_scan(wdn, dn_bytes, sdn, sdn_bytes, cfg->weight_dtype, flag, st)) !=
+              cudaSuccess ||
+          (e = cudaMemcpyAsync(&general, flag, sizeof(int), cudaMemcpyDeviceToHost, st)) !=
+              cudaSuccess ||
+          (e = cudaStreamSynchronize(st)) != cudaSuccess)
+        return bail(COLI_ECUDA, "MX weight scan", e);
+    }
+    if ((e = tc_plan_create(&h->tc, cfg->weight_dtype, wgu, wdn, sgu, sdn, E, d, f,
+                            static_cast<int>(Na), h->x_perm, h->H, general != 0)) != cudaSuccess)
       return bail(COLI_ECUDA, "tensor-core plan", e);
   }
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return bail(COLI_ECUDA, "create sync", e);

@@ -81,6 +81,12 @@ COLI_DEV uint4 lds128(uint32_t addr) {
   return v;
 }
 
+COLI_DEV uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
 // ---- warp-level tensor-core MMA (m16n8k16, bf16 in, fp32 accumulate) --------
 COLI_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                              uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -178,5 +184,28 @@ COLI_DEV uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
 }
 
 COLI_DEV uint32_t lane_id() { return threadIdx.x & 31u; }
+
+// ---- OCP Microscaling element codes ------------------------------------------
+// Every E4M3 and E2M1 value is exact in fp16; the hardware converts two codes
+// to an fp16 pair in one instruction.
+// 8 E4M3 codes (two words, lower address first) -> four fp16 pairs.
+COLI_DEV void e4m3x8_f16(uint32_t w0, uint32_t w1, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b16 a, b, c, d;\n\t"
+      "mov.b32 {a, b}, %4;\n\tmov.b32 {c, d}, %5;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %2, c;\n\tcvt.rn.f16x2.e4m3x2 %3, d;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w0), "r"(w1));
+}
+
+// 8 E2M1 codes (one word, low nibble = even index) -> four fp16 pairs.
+COLI_DEV void e2m1x8_f16(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 a, b, c, d;\n\t"
+      "mov.b32 {a, b, c, d}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, a;\n\tcvt.rn.f16x2.e2m1x2 %1, b;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, c;\n\tcvt.rn.f16x2.e2m1x2 %3, d;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
 
 }  // namespace coli

@@ -123,19 +123,43 @@ cudaError_t launch_repack_mx(const void* src_gate, const void* src_up, const voi
                              int d, int f, void* dst_gu, void* dst_sgu, void* dst_dn,
                              void* dst_sdn, cudaStream_t st);
 
-// Prefill path: TMA + tcgen05/TMEM grouped GEMM (bf16 or int4 weights).
+// Prefill path: TMA + tcgen05/TMEM grouped GEMM. bf16 weights: both operands
+// in shared memory (CTA pairs); int4 / MX weights: dequantised into tensor
+// memory by converter warps (k_ffn_tcq.cu).
 struct TcPlan;  // defined in k_ffn_tc.cu
-bool tc_supported(int d, int f);
+struct QPlan;   // defined in k_ffn_tcq.cu
+// Whether a layer of this weight format and shape has a tensor-core plan.
+bool tc_supported(int wdt, int d, int f);
+bool tcq_supported(int wdt, int d, int f);
+// 2-D tensor map [rows][cols] of elem_bytes-wide elements, box box_rows x box_cols.
+cudaError_t encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr,
+                           uint64_t rows, uint64_t cols, int box_cols, int box_rows,
+                           CUtensorMapSwizzle swizzle);
 // x_perm [max_rows][d] and H [max_rows][f] are the handle's buffers: their
 // tensor maps are encoded once here (rows past a forward's last group are
 // computed from stale data but never stored).
-// wdt DT_BF16: w_gu/w_dn bf16 in the handle layout; DT_I4G128: int4 bytes
-// plus bf16 scales s_gu/s_dn (rounded to bf16 per weight when dequantised
-// for the tensor cores).
+// wdt DT_BF16: w_gu/w_dn bf16 in the handle layout. DT_I4G128: int4 bytes
+// plus bf16 scales s_gu/s_dn (q * s rounded to bf16 per weight). DT_MXFP8 /
+// DT_MXFP4: MX bytes in the decode layout plus E8M0 scales (exact in bf16
+// within its range); mx_general: the weights hold E4M3 NaN codes or scales
+// above 2^15, which take the exact fp32 conversion.
 cudaError_t tc_plan_create(TcPlan** plan, int wdt, const void* w_gu, const void* w_dn,
-                           const __nv_bfloat16* s_gu, const __nv_bfloat16* s_dn, int E, int d,
-                           int f, int max_rows, const void* x_perm, const void* H);
+                           const void* s_gu, const void* s_dn, int E, int d, int f, int max_rows,
+                           const void* x_perm, const void* H, bool mx_general);
 void tc_plan_destroy(TcPlan* plan);
+cudaError_t tcq_plan_create(QPlan** plan, int wdt, const void* w_gu, const void* w_dn,
+                            const void* s_gu, const void* s_dn, int E, int d, int f,
+                            int max_rows, const void* x_perm, const void* H, bool general);
+void tcq_plan_destroy(QPlan* plan);
+cudaError_t launch_tcq_gateup(QPlan* p, const void* x_perm, bool own_x_perm,
+                              const int32_t* offsets, void* H, int n_rows, cudaStream_t st,
+                              int* status);
+cudaError_t launch_tcq_down(QPlan* p, const int32_t* offsets, void* y_perm, bool bf16_out,
+                            int n_rows, cudaStream_t st, int* status);
+// Sets *flag (device int) to 1 when MX weights hold E4M3 NaN codes
+// (MXFP8) or scale bytes above 142.
+cudaError_t launch_mx_scan(const void* w, size_t w_bytes, const void* s, size_t s_bytes, int wdt,
+                           int* flag, cudaStream_t st);
 // H[rows][f] = silu(x_perm Wg^T) * (x_perm Wu^T) per expert group (bf16).
 // own_x_perm: x_perm is the plan's buffer (its map is reused), else a map is
 // encoded for this call.

@@ -36,26 +36,6 @@ constexpr int kMaxRowsPerPass = 16;  // token rows per weight pass (two 8-token 
 template <int FMT>
 constexpr int kLaneStep = FMT == 8 ? 32 : 16;  // bytes of one row per lane and 128-index step
 
-// 8 E4M3 codes (two words, lower address first) -> four fp16 pairs.
-COLI_DEV void e4m3x8_f16(uint32_t w0, uint32_t w1, uint32_t (&o)[4]) {
-  asm("{\n\t.reg .b16 a, b, c, d;\n\t"
-      "mov.b32 {a, b}, %4;\n\tmov.b32 {c, d}, %5;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %2, c;\n\tcvt.rn.f16x2.e4m3x2 %3, d;\n\t}"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-      : "r"(w0), "r"(w1));
-}
-
-// 8 E2M1 codes (one word, low nibble = even index) -> four fp16 pairs.
-COLI_DEV void e2m1x8_f16(uint32_t w, uint32_t (&o)[4]) {
-  asm("{\n\t.reg .b8 a, b, c, d;\n\t"
-      "mov.b32 {a, b, c, d}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, a;\n\tcvt.rn.f16x2.e2m1x2 %1, b;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, c;\n\tcvt.rn.f16x2.e2m1x2 %3, d;\n\t}"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-      : "r"(w));
-}
-
 COLI_DEV void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                       uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
@@ -416,6 +396,31 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Flags weights outside the prefill converters' fast conversion: E4M3 NaN
+// codes (any byte whose low seven bits are all ones) and scale bytes above
+// 142 (scales beyond 2^15, NaN included).
+__global__ void __launch_bounds__(256)
+    k_mx_scan(const uint4* __restrict__ w, size_t w_vec, const uint4* __restrict__ s,
+              size_t s_vec, int* flag) {
+  bool hit = false;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < w_vec;
+       i += stride) {
+    const uint4 v = w[i];
+    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) hit |= (((x[j] & 0x7f7f7f7fu) + 0x01010101u) & 0x80808080u) != 0u;
+  }
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < s_vec;
+       i += stride) {
+    const uint4 v = s[i];
+    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) hit |= __vcmpgtu4(x[j], 0x8e8e8e8eu) != 0u;
+  }
+  if (__any_sync(0xffffffffu, hit) && (threadIdx.x & 31) == 0) *flag = 1;
+}
+
 }  // namespace
 
 int mx_blocks_per_sm(int wdt) {
@@ -506,6 +511,15 @@ cudaError_t launch_repack_mx(const void* src_gate, const void* src_up, const voi
                                          true, static_cast<uint8_t*>(dst_sgu));
   k_repack_rows_u8<<<grid, 256, 0, st>>>(static_cast<const uint8_t*>(sd), nullptr, d, d, f / 32,
                                          E, false, static_cast<uint8_t*>(dst_sdn));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_scan(const void* w, size_t w_bytes, const void* s, size_t s_bytes, int wdt,
+                           int* flag, cudaStream_t st) {
+  // E2M1 has no NaN code: only the scales are scanned
+  const size_t wv = wdt == DT_MXFP8 ? w_bytes / 16 : 0, sv = s_bytes / 16;
+  k_mx_scan<<<1024, 256, 0, st>>>(static_cast<const uint4*>(w), wv,
+                                  static_cast<const uint4*>(s), sv, flag);
   return cudaGetLastError();
 }
 

@@ -1,4 +1,6 @@
-// A3, prefill path: grouped expert GEMM on the 5th-generation tensor cores.
+// A3, prefill path: grouped expert GEMM on the 5th-generation tensor cores,
+// bf16 expert weights (int4 and MX experts: k_ffn_tcq.cu, which dequantises
+// the weights into tensor memory).
 //
 // For groups of hundreds of rows per expert the FFN is a dense contraction
 // (per expert: rows x d x 2f for gate/up, rows x f x d for down), so it runs
@@ -40,37 +42,26 @@ namespace coli {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int A_BYTES = BM * BK * 2;    // 16 KiB
-constexpr int B_BYTES = BN * BK * 2;    // 32 KiB
-constexpr int RAW_BYTES = BN * BK / 2;  // 8 KiB of int4 weights per stage
+constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KiB
 constexpr int TMEM_COLS = 512;
 constexpr int kMaxE = 256;
-constexpr int kMaxStages = 4;
-
-// Warp roles: 0 TMA, 1 MMA (+ TMEM alloc), 2-5 epilogue; int4 adds 6-9,
-// the converters (one per SM sub-partition: warp w issues on w % 4).
-template <bool I4>
-struct Shape {
-  static constexpr int kStages = I4 ? 3 : 4;
-  static constexpr int kThreads = I4 ? 320 : 192;
-  static constexpr int kStageBytes = A_BYTES + B_BYTES + (I4 ? RAW_BYTES : 0);
-};
+constexpr int STAGES = 4;
+constexpr int kThreads = 192;  // warps: 0 TMA, 1 MMA (+ TMEM alloc), 2-5 epilogue
+constexpr int kStageBytes = A_BYTES + B_BYTES;
 
 // bf16 x bf16 -> fp32, A and B K-major, M = 128, N = 256.
 constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
 
 struct __align__(8) Ctrl {
-  uint64_t full[kMaxStages], empty[kMaxStages], rawfull[kMaxStages], tfull[2], tempty[2];
+  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
   uint32_t tmem_base;
   int abort;
   int tile_off[kMaxE + 1];  // first tile of expert e
   int row_off[kMaxE + 1];   // first row of expert e (the offsets)
 };
 
-template <bool I4>
-constexpr size_t smem_bytes() {
-  return 1024 + Shape<I4>::kStages * Shape<I4>::kStageBytes + sizeof(Ctrl);
-}
+constexpr size_t kSmem = 1024 + STAGES * kStageBytes + sizeof(Ctrl);
 
 struct Tile {
   int e, nt, mt;
@@ -89,73 +80,19 @@ COLI_DEV Tile decode_tile(const Ctrl& C, int E, int n_tiles_n, int t) {
   return Tile{lo, local / mts, local % mts};
 }
 
-COLI_DEV void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-
-// int4 weights of the B tile: scale of one weight row for one 128-index
-// group (0 for rows past the end of the tensor, whose bytes TMA zero-fills).
-struct I4Args {
-  const __nv_bfloat16* scales;  // [weight rows][K/128]
-  int groups;                   // K / 128
-  int total_rows;               // weight rows in the tensor (E * N)
-};
-
-COLI_DEV uint32_t scale_pair(const I4Args& q, int row, int g) {
-  if (row >= q.total_rows) return 0u;
-  const uint32_t s = __bfloat16_as_ushort(q.scales[static_cast<size_t>(row) * q.groups + g]);
-  return s | (s << 16);
-}
-
-// One converter thread's share of a stage: weight rows r and r + 128 of the
-// 256-row tile, 64 reduction indices each (32 int4 bytes in `raw`, rows 32
-// bytes apart), written as bf16 into the 128-byte-swizzled K-major operand
-// `b` (row r at r * 128; its 16-byte chunk j at chunk j ^ (r % 8)). Each
-// weight is q * s rounded once to bf16: 136 + q from the nibble (LOP3), minus
-// 136 (exact), times the group scale (one rounding).
-COLI_DEV void convert_rows(uint32_t raw, uint32_t b, int ct, const uint32_t (&s2)[2]) {
-  constexpr uint32_t kOne = 0x3F803F80u, kMinus136 = 0xC308C308u, kMinusZero = 0x80008000u;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = ct + 128 * h;
-    const int c0 = (r >> 2) & 1;  // eight rows of a quarter-warp hit distinct banks
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int c = c0 ^ cc;
-      const uint4 v = lds128(raw + r * 32 + c * 16);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t w = word_of(v, i);
-        uint32_t o[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-          o[p] = fma_bf16x2(fma_bf16x2(nib_pair136(w, p), kOne, kMinus136), s2[h], kMinusZero);
-        const int j = c * 4 + i;
-        sts128(b + r * 128 + ((j ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
-      }
-    }
-  }
-}
-
 // EPI 0: gate/up + SwiGLU -> bf16 H [rows][N/2]; EPI 1: fp32 out [rows][N];
 // EPI 2: bf16 out [rows][N].
-// I4: map_b is the int4 weight tensor (bytes [rows][K/2], box 256 x 32) and
-// the B operand is dequantised in shared memory by the converter warps.
-template <int EPI, bool I4>
-__global__ void __launch_bounds__(Shape<I4>::kThreads, 1)
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
               const int32_t* __restrict__ offsets, int E, int K, int N, void* __restrict__ out,
-              I4Args q4, int* status) {
-  constexpr int STAGES = Shape<I4>::kStages;
+              int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sa = smem_u32(base);
   const uint32_t sb = sa + STAGES * A_BYTES;
-  const uint32_t sraw = sb + STAGES * B_BYTES;  // int4 only
-  Ctrl& C = *reinterpret_cast<Ctrl*>(base + STAGES * Shape<I4>::kStageBytes);
+  Ctrl& C = *reinterpret_cast<Ctrl*>(base + STAGES * kStageBytes);
   volatile int* abort = &C.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t deadline = global_timer_ns() + kWaitTimeoutNs;
@@ -195,10 +132,8 @@ __global__ void __launch_bounds__(Shape<I4>::kThreads, 1)
     if (lane == 31) C.tile_off[E] = incl;  // all tiles
     if (lane == 0) {
       for (int s = 0; s < STAGES; ++s) {
-        // full: the producer's expect_tx, plus one arrival per converter warp
-        mbar_init(smem_u32(&C.full[s]), I4 ? 5 : 1);
+        mbar_init(smem_u32(&C.full[s]), 1);
         mbar_init(smem_u32(&C.empty[s]), 1);
-        mbar_init(smem_u32(&C.rawfull[s]), 1);
       }
       for (int a = 0; a < 2; ++a) {
         mbar_init(smem_u32(&C.tfull[a]), 1);
@@ -225,21 +160,12 @@ __global__ void __launch_bounds__(Shape<I4>::kThreads, 1)
         const int a_row = C.row_off[tl.e] + tl.mt * BM;
         const int b_row = tl.e * N + tl.nt * BN;
         for (int kb = 0; kb < kblocks; ++kb) {
-          // a free slot: the MMA of its last use has completed (so have the
-          // converters' reads of its raw bytes, which came before that MMA)
+          // a free slot: the MMA of its last use has completed
           if (!wait_bar(smem_u32(&C.empty[stage]), phase ^ 1u, deadline, abort)) break;
           const uint32_t fb = smem_u32(&C.full[stage]);
-          if constexpr (I4) {
-            mbar_arrive_expect_tx(fb, A_BYTES);
-            tma_load_2d(sa + stage * A_BYTES, &map_a, fb, kb * BK, a_row);
-            const uint32_t rb = smem_u32(&C.rawfull[stage]);
-            mbar_arrive_expect_tx(rb, RAW_BYTES);
-            tma_load_2d(sraw + stage * RAW_BYTES, &map_b, rb, kb * (BK / 2), b_row);
-          } else {
-            mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-            tma_load_2d(sa + stage * A_BYTES, &map_a, fb, kb * BK, a_row);
-            tma_load_2d(sb + stage * B_BYTES, &map_b, fb, kb * BK, b_row);
-          }
+          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
+          tma_load_2d(sa + stage * A_BYTES, &map_a, fb, kb * BK, a_row);
+          tma_load_2d(sb + stage * B_BYTES, &map_b, fb, kb * BK, b_row);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -355,46 +281,6 @@ __global__ void __launch_bounds__(Shape<I4>::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&C.tempty[acc]));
-    }
-  } else if constexpr (I4) {  // ---- converters: warps 6..9, int4 -> bf16 B operand
-    const int ct = threadIdx.x - 192;  // 0..127
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
-      const Tile tl = decode_tile(C, E, n_tiles_n, t);
-      const int b_row = tl.e * N + tl.nt * BN;
-      // scales of this thread's two rows: the current group's, and the next
-      // group's requested a group ahead
-      uint32_t s2[2], s2n[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) s2n[h] = s2[h] = scale_pair(q4, b_row + ct + 128 * h, 0);
-      bool ok = true;
-      for (int kb = 0; kb < kblocks; ++kb) {
-        const int g = kb / (128 / BK);
-        if (kb % (128 / BK) == 0 && g + 1 < q4.groups) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) s2n[h] = scale_pair(q4, b_row + ct + 128 * h, g + 1);
-        }
-        if (!__all_sync(0xffffffffu,
-                        wait_bar(smem_u32(&C.rawfull[stage]), phase, deadline, abort))) {
-          ok = false;
-          break;
-        }
-        convert_rows(sraw + stage * RAW_BYTES, sb + stage * B_BYTES, ct, s2);
-        // the MMA reads the operand through the async proxy
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&C.full[stage]));
-        if (kb % (128 / BK) == (128 / BK) - 1) {
-          s2[0] = s2n[0];
-          s2[1] = s2n[1];
-        }
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-      if (!ok) break;
     }
   }
 
@@ -716,67 +602,61 @@ cudaError_t encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_byte
 
 struct TcPlan {
   CUtensorMap map_wgu, map_wdn, map_xperm, map_h;
-  bool i4;
-  bool pair;  // bf16 weights: CTA-pair kernel with half-height weight maps
-  const __nv_bfloat16 *s_gu, *s_dn;  // int4 scales [rows][K/128]
+  bool pair;           // CTA-pair kernel with half-height weight maps
+  QPlan* q = nullptr;  // int4 / MX weights: the tensor-memory-operand kernel
   int E, d, f, grid;
 };
 
-bool tc_supported(int d, int f) { return d % 64 == 0 && f % 64 == 0 && encode_fn() != nullptr; }
-
-// int4 weights as bytes [rows][K/2]: box of 256 rows x 32 bytes (64 indices),
-// no swizzle (the converters read rows 32 bytes apart).
-static cudaError_t make_i4_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K) {
-  return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, ptr, rows, K / 2, BK / 2, BN,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
+bool tc_supported(int wdt, int d, int f) {
+  if (encode_fn() == nullptr) return false;
+  if (wdt == DT_BF16) return d % 64 == 0 && f % 64 == 0;
+  return tcq_supported(wdt, d, f);
 }
 
-template <int EPI, bool I4>
+template <int EPI>
 static cudaError_t set_smem() {
-  return cudaFuncSetAttribute(k_tc_gemm<EPI, I4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(smem_bytes<I4>()));
+  return cudaFuncSetAttribute(k_tc_gemm<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kSmem));
 }
 
 cudaError_t tc_plan_create(TcPlan** plan, int wdt, const void* w_gu, const void* w_dn,
-                           const __nv_bfloat16* s_gu, const __nv_bfloat16* s_dn, int E, int d,
-                           int f, int max_rows, const void* x_perm, const void* H) {
+                           const void* s_gu, const void* s_dn, int E, int d, int f, int max_rows,
+                           const void* x_perm, const void* H, bool mx_general) {
   *plan = nullptr;
   TcPlan* p = new TcPlan();
   p->E = E;
   p->d = d;
   p->f = f;
-  p->i4 = wdt == DT_I4G128;
-  p->s_gu = s_gu;
-  p->s_dn = s_dn;
-  int dev = 0, sms = 0;
   cudaError_t e;
+  if (wdt != DT_BF16) {
+    e = tcq_plan_create(&p->q, wdt, w_gu, w_dn, s_gu, s_dn, E, d, f, max_rows, x_perm, H,
+                        mx_general);
+    if (e != cudaSuccess) {
+      delete p;
+      return e;
+    }
+    *plan = p;
+    return cudaSuccess;
+  }
+  int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
       (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
     delete p;
     return e;
   }
-  p->grid = sms;
-  if (p->i4) {
-    e = make_i4_map(&p->map_wgu, w_gu, static_cast<uint64_t>(E) * 2 * f, d);
-    if (e == cudaSuccess) e = make_i4_map(&p->map_wdn, w_dn, static_cast<uint64_t>(E) * d, f);
-    if (e == cudaSuccess) e = set_smem<0, true>();
-    if (e == cudaSuccess) e = set_smem<1, true>();
-    if (e == cudaSuccess) e = set_smem<2, true>();
-  } else {
-    // each CTA of a pair loads 128 of the 256 weight rows of a tile
-    p->pair = sms >= 2;
-    const int box = p->pair ? BN / 2 : BN;
-    e = make_map(&p->map_wgu, w_gu, static_cast<uint64_t>(E) * 2 * f, d, box);
-    if (e == cudaSuccess) e = make_map(&p->map_wdn, w_dn, static_cast<uint64_t>(E) * d, f, box);
-    if (e == cudaSuccess) e = set_smem<0, false>();
-    if (e == cudaSuccess) e = set_smem<1, false>();
-    if (e == cudaSuccess) e = set_smem<2, false>();
-    for (auto fn : {k_tc_gemm_pair<0>, k_tc_gemm_pair<1>, k_tc_gemm_pair<2>})
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kPairSmem));
-    if (p->pair) p->grid = sms & ~1;  // whole pairs
-  }
+  // each CTA of a pair loads 128 of the 256 weight rows of a tile
+  p->pair = sms >= 2;
+  p->grid = p->pair ? sms & ~1 : sms;  // whole pairs
+  const int box = p->pair ? BN / 2 : BN;
+  e = make_map(&p->map_wgu, w_gu, static_cast<uint64_t>(E) * 2 * f, d, box);
+  if (e == cudaSuccess) e = make_map(&p->map_wdn, w_dn, static_cast<uint64_t>(E) * d, f, box);
+  if (e == cudaSuccess) e = set_smem<0>();
+  if (e == cudaSuccess) e = set_smem<1>();
+  if (e == cudaSuccess) e = set_smem<2>();
+  for (auto fn : {k_tc_gemm_pair<0>, k_tc_gemm_pair<1>, k_tc_gemm_pair<2>})
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kPairSmem));
   if (e == cudaSuccess) e = make_map(&p->map_xperm, x_perm, static_cast<uint64_t>(max_rows), d, BM);
   if (e == cudaSuccess) e = make_map(&p->map_h, H, static_cast<uint64_t>(max_rows), f, BM);
   if (e != cudaSuccess) {
@@ -787,26 +667,27 @@ cudaError_t tc_plan_create(TcPlan** plan, int wdt, const void* w_gu, const void*
   return cudaSuccess;
 }
 
-void tc_plan_destroy(TcPlan* plan) { delete plan; }
+void tc_plan_destroy(TcPlan* plan) {
+  if (plan && plan->q) tcq_plan_destroy(plan->q);
+  delete plan;
+}
 
 template <int EPI>
 static void launch(const TcPlan* p, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                   const int32_t* offsets, int K, int N, void* out, I4Args q4, cudaStream_t st,
+                   const int32_t* offsets, int K, int N, void* out, cudaStream_t st,
                    int* status) {
   if (p->pair)
     k_tc_gemm_pair<EPI><<<p->grid, 192, kPairSmem, st>>>(map_a, map_b, offsets, p->E, K, N, out,
                                                          status);
-  else if (p->i4)
-    k_tc_gemm<EPI, true><<<p->grid, Shape<true>::kThreads, smem_bytes<true>(), st>>>(
-        map_a, map_b, offsets, p->E, K, N, out, q4, status);
   else
-    k_tc_gemm<EPI, false><<<p->grid, Shape<false>::kThreads, smem_bytes<false>(), st>>>(
-        map_a, map_b, offsets, p->E, K, N, out, q4, status);
+    k_tc_gemm<EPI><<<p->grid, kThreads, kSmem, st>>>(map_a, map_b, offsets, p->E, K, N, out,
+                                                     status);
 }
 
 cudaError_t launch_tc_gateup(TcPlan* p, const void* x_perm, bool own_x_perm,
                              const int32_t* offsets, void* H, int n_rows, cudaStream_t st,
                              int* status) {
+  if (p->q) return launch_tcq_gateup(p->q, x_perm, own_x_perm, offsets, H, n_rows, st, status);
   if (n_rows == 0) return cudaSuccess;
   CUtensorMap map_a;
   if (own_x_perm) {
@@ -815,20 +696,19 @@ cudaError_t launch_tc_gateup(TcPlan* p, const void* x_perm, bool own_x_perm,
     const cudaError_t e = make_map(&map_a, x_perm, static_cast<uint64_t>(n_rows), p->d, BM);
     if (e != cudaSuccess) return e;
   }
-  const I4Args q4{p->s_gu, p->d / 128, p->E * 2 * p->f};
-  launch<0>(p, map_a, p->map_wgu, offsets, p->d, 2 * p->f, H, q4, st, status);
+  launch<0>(p, map_a, p->map_wgu, offsets, p->d, 2 * p->f, H, st, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_tc_down(TcPlan* p, const void* H, const int32_t* offsets, void* y_perm,
                            bool bf16_out, int n_rows, cudaStream_t st, int* status) {
   (void)H;  // always the plan's H buffer, mapped at create
+  if (p->q) return launch_tcq_down(p->q, offsets, y_perm, bf16_out, n_rows, st, status);
   if (n_rows == 0) return cudaSuccess;
-  const I4Args q4{p->s_dn, p->f / 128, p->E * p->d};
   if (bf16_out)
-    launch<2>(p, p->map_h, p->map_wdn, offsets, p->f, p->d, y_perm, q4, st, status);
+    launch<2>(p, p->map_h, p->map_wdn, offsets, p->f, p->d, y_perm, st, status);
   else
-    launch<1>(p, p->map_h, p->map_wdn, offsets, p->f, p->d, y_perm, q4, st, status);
+    launch<1>(p, p->map_h, p->map_wdn, offsets, p->f, p->d, y_perm, st, status);
   return cudaGetLastError();
 }
 

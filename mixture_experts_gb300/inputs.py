@@ -88,8 +88,9 @@ class MoEShape:
 
 # The five workloads: a tiny fp32 layer; a Mixtral-8x7B-shaped layer at a
 # decode batch and at prefill (8 sequences x 512 tokens); a fine-grained
-# 256-expert layer with int4 experts; a skewed-routing stress layer. One more
-# measures int4 experts at a prefill batch.
+# 256-expert layer with int4 experts; a skewed-routing stress layer. The
+# others measure quantised experts (int4, MX) at decode and prefill batches
+# and the residency tier.
 CONFIGS = {
     "tiny_fp32": MoEShape("tiny_fp32", T=64, d=256, E=8, k=2, f=512, act="f32", wdt="f32"),
     "mixtral_decode": MoEShape("mixtral_decode", T=32, d=4096, E=8, k=2, f=14336),
@@ -97,13 +98,17 @@ CONFIGS = {
     "fine_int4": MoEShape("fine_int4", T=256, d=6144, E=256, k=8, f=2048, wdt="i4g128"),
     "skewed": MoEShape("skewed", T=16384, d=2048, E=64, k=4, f=1408, bias="zipf"),
     # beside the five: the Mixtral-shaped prefill layer with int4 g128
-    # experts (~1024 rows per expert), for the int4 tensor-core GEMM; and the
-    # two decode layers with block-scaled (OCP MX) experts
+    # experts (~1024 rows per expert), for the quantised tensor-core GEMM; and
+    # the two decode layers with block-scaled (OCP MX) experts
     "mixtral_prefill_int4": MoEShape("mixtral_prefill_int4", T=4096, d=4096, E=8, k=2,
                                      f=14336, wdt="i4g128"),
     "mixtral_decode_mxfp8": MoEShape("mixtral_decode_mxfp8", T=32, d=4096, E=8, k=2, f=14336,
                                      wdt="mxfp8"),
     "fine_mxfp4": MoEShape("fine_mxfp4", T=256, d=6144, E=256, k=8, f=2048, wdt="mxfp4"),
+    # the Mixtral-shaped prefill layer with MXFP8 experts (tensor-core GEMM
+    # with the weights dequantised into tensor memory)
+    "mixtral_prefill_mxfp8": MoEShape("mixtral_prefill_mxfp8", T=4096, d=4096, E=8, k=2,
+                                      f=14336, wdt="mxfp8"),
     # the decode layer with its experts in host memory and 2 of 8 in HBM:
     # 6 active experts stream over NVLink-C2C every forward
     "mixtral_decode_tier": MoEShape("mixtral_decode_tier", T=32, d=4096, E=8, k=2, f=14336,

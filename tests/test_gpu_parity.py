@@ -35,6 +35,11 @@ SMALL = {
     "mxfp8": S("mxfp8", T=40, d=512, E=8, k=2, f=256, wdt="mxfp8"),
     "mxfp4": S("mxfp4", T=60, d=384, E=6, k=3, f=384, wdt="mxfp4"),
     "mxfp8_bias": S("mxfp8_bias", T=90, d=256, E=16, k=4, f=128, wdt="mxfp8", bias="zipf"),
+    # MX experts with hundreds of rows each: the tensor-core GEMM with the
+    # weights dequantised into tensor memory (ragged K: 384 = one and a half
+    # E2M1 slots; f = 640: odd weight-tile count)
+    "mxfp8_prefill": S("mxfp8_prefill", T=700, d=384, E=5, k=2, f=640, wdt="mxfp8"),
+    "mxfp4_prefill": S("mxfp4_prefill", T=800, d=384, E=6, k=3, f=640, wdt="mxfp4"),
 }
 
 
@@ -62,7 +67,8 @@ def test_forward_small(name):
     check_layer(s, lay, y, dbg)
 
 
-@pytest.mark.parametrize("name", ["decode_bf16", "prefill_bf16", "skew_small", "int4_prefill"])
+@pytest.mark.parametrize("name", ["decode_bf16", "prefill_bf16", "skew_small", "int4_prefill",
+                                  "mxfp8_prefill", "mxfp4_prefill"])
 def test_paths_agree(name):
     """Decode (weight streaming) and prefill (tcgen05 grouped GEMM) paths give
     the same routing and outputs within rounding on the same inputs."""
@@ -118,6 +124,17 @@ def test_full_mx_layers(name):
     assert layer.path_for(s.T) == moe.PATH_DECODE
     err, near = check_layer(s, lay, y, dbg, threads=os.cpu_count() or 1)
     print(f"{name}: rel_err={err:.3e} near_ties={near} tokens_checked={s.T - near}")
+
+
+def test_full_mxfp8_prefill_layer_sampled():
+    """The Mixtral-shaped layer with MXFP8 experts at the prefill batch:
+    routing and dispatch of every token, outputs of 512 seeded tokens."""
+    s = inputs.CONFIGS["mixtral_prefill_mxfp8"]
+    lay = inputs.make_layer(s, seed=0)
+    layer, y, dbg = run_layer(s, lay)
+    assert layer.path_for(s.T) == moe.PATH_PREFILL
+    err, near = check_layer(s, lay, y, dbg, threads=os.cpu_count() or 1, sample=512)
+    print(f"mixtral_prefill_mxfp8: rel_err={err:.3e} near_ties={near}")
 
 
 def test_full_int4_prefill_layer_sampled():
@@ -315,6 +332,52 @@ def test_int4_prefill_many_tiles_per_cta():
     assert layer.path_for(s.T) == moe.PATH_PREFILL
     err, near = check_layer(s, lay, y, dbg, threads=os.cpu_count() or 1)
     print(f"int4_wrap: rel_err={err:.3e} near_ties={near}")
+
+
+@pytest.mark.parametrize("wdt", ["mxfp8", "mxfp4"])
+def test_mx_prefill_many_tiles_per_cta(wdt):
+    """MX experts on the tensor-core path with several tiles per CTA (the raw
+    slots and tensor-memory stages wrap across tiles): every token."""
+    s = S(f"{wdt}_wrap", T=3000, d=1024, E=8, k=2, f=1536, wdt=wdt)
+    lay = inputs.make_layer(s, seed=44)
+    layer, y, dbg = run_layer(s, lay)
+    assert layer.path_for(s.T) == moe.PATH_PREFILL
+    err, near = check_layer(s, lay, y, dbg, threads=os.cpu_count() or 1)
+    print(f"{s.name}: rel_err={err:.3e} near_ties={near}")
+
+
+@pytest.mark.parametrize("wdt", ["mxfp8", "mxfp4"])
+def test_mx_prefill_special_values(wdt):
+    """MX weights outside the converters' fast range, on the tensor-core
+    path: block scales of 2^16 and 2^30 and a NaN scale (and, for E4M3, NaN
+    codes) take the exact fp32 conversion; outputs are NaN exactly where the
+    oracle's are and match it elsewhere."""
+    s = S(f"{wdt}_special", T=300, d=256, E=4, k=2, f=256, wdt=wdt)
+    lay = inputs.make_layer(s, seed=45)
+    sg = lay["s_gate"].clone()
+    sg[0, 3, 1] = 127 + 16          # one gate block of expert 0 scaled by 2^16 more
+    sg[1, 5, 0] = 127 + 30
+    lay["s_gate"] = sg
+    sd = lay["s_down"].clone()
+    sd[2, 7, 2] = 255               # NaN scale: one block of down row 7 of expert 2
+    lay["s_down"] = sd
+    if wdt == "mxfp8":
+        wd = lay["w_down"].clone()
+        wd[3, 11, 40] = 0x7F        # E4M3 NaN code in down row 11 of expert 3
+        lay["w_down"] = wd
+    layer, y, dbg = run_layer(s, lay, path=moe.PATH_PREFILL)
+    assert layer.path_for(s.T) == moe.PATH_PREFILL
+    idx, w, gap, inner = oracle_routing(s, lay)
+    near = check_routing(dbg["topk_idx"], dbg["topk_w"], idx, w, gap, inner)
+    tokens = np.nonzero(~near)[0].astype(np.int32)
+    ref = oracle.moe_forward(lay, s.act_code, s.w_code, s.T, s.d, s.E, s.k, s.f,
+                             tokens=tokens)["y_f64"]
+    got = y_to_f64(y)[tokens]
+    assert np.isnan(ref).any()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    err = np.max(np.abs(got[fin] - ref[fin])) / np.max(np.abs(ref[fin]))
+    assert err <= TOL[wdt], err
 
 
 def test_empty_batch_is_a_no_op():
