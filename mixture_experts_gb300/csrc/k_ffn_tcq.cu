@@ -5,9 +5,10 @@
 // The expert weights arrive quantised, so every weight has to become bf16
 // before the tensor core can multiply it, and that conversion, not the MMA,
 // is what the kernel is built around. A tile is 128 weight rows x 256 token
-// rows. Four converter warps turn the tile's 128 weight rows of each
-// 64-index stage into bf16 pairs in registers and write them straight into
-// tensor memory (tcgen05.st), where tcgen05.mma reads them as its A operand;
+// rows. Eight converter warps (two per lane quarter, alternate stages) turn
+// the tile's 128 weight rows of each 64-index stage into bf16 pairs in
+// registers and write them straight into tensor memory (tcgen05.st), where
+// tcgen05.mma reads them as its A operand;
 // TMA brings the 256 activation rows (bf16, 128-byte swizzle) into shared
 // memory as the B operand; the fp32 accumulator D[weight row][token] takes
 // 256 tensor-memory columns beside four 32-column A stages. Per stage the
@@ -86,7 +87,8 @@ constexpr int D_COL = 0;                  // accumulator: 256 fp32 columns
 constexpr int A_COL = 256;                // A stages: BK / 2 columns of bf16 pairs each
 constexpr int TMEM_COLS = 512;
 constexpr int kEpiWarps = 8;             // two per lane quarter, half the columns each
-constexpr int kThreads = 32 * (2 + kEpiWarps + 4);  // warps: 0 TMA, 1 MMA, epilogue, converters
+constexpr int kConvWarps = 8;            // two per lane quarter, alternate stages
+constexpr int kThreads = 32 * (2 + kEpiWarps + kConvWarps);  // 0 TMA, 1 MMA, epilogue, converters
 constexpr int kConv0 = 2 + kEpiWarps;     // first converter warp
 constexpr int kMaxE = 256;
 
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int s = 0; s < SLOTS; ++s) {
         mbar_init(smem_u32(&C.rawfull[s]), 1);
-        mbar_init(smem_u32(&C.rawempty[s]), 4);
+        mbar_init(smem_u32(&C.rawempty[s]), kConvWarps);
       }
       mbar_init(smem_u32(&C.tfull), 1);
       mbar_init(smem_u32(&C.tempty), kEpiWarps);
@@ -439,8 +441,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&C.tempty));
     }
-  } else {  // ---- converters: the last four warps, weights -> bf16 A operand in tensor memory
+  } else {  // ---- converters: the last eight warps, weights -> bf16 A operand in tensor memory
+    // two warps per lane quarter take alternate stages, so one's conversion
+    // overlaps the other's tensor-memory store and barrier round trip
     const int q = warp & 3;
+    const int g = (warp - kConv0) >> 2;  // stage parity this warp converts
     const int rr = lane_row<EPI>(q, lane);
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + A_COL;
     int stage = 0, slot = 0;
@@ -455,30 +460,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int kb = 0; kb < kblocks; ++kb) {
         const int sub = kb % SUBS;
+        const bool last = sub == SUBS - 1 || kb == kblocks - 1;  // the slot's last stage
         if (sub == 0 && kb > 0) {
           sc[0] = scn[0];
           sc[1] = scn[1];
           slot_scales<WQ>(qa, row, K, kb / SUBS + 1, scn);
         }
-        // the A stage is free once the MMA that read it completed; the raw
-        // slot holds this stage's weights
-        if (!__all_sync(0xffffffffu,
-                        wait_bar(smem_u32(&C.empty[stage]), phase ^ 1u, deadline, abort) &&
-                            wait_bar(smem_u32(&C.rawfull[slot]), sphase, deadline, abort))) {
-          ok = false;
-          break;
+        if ((stage & 1) == g) {
+          // the A stage is free once the MMA that read it completed; the raw
+          // slot holds this stage's weights
+          if (!__all_sync(0xffffffffu,
+                          wait_bar(smem_u32(&C.empty[stage]), phase ^ 1u, deadline, abort) &&
+                              wait_bar(smem_u32(&C.rawfull[slot]), sphase, deadline, abort))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t o[32];
+          const uint32_t rowp = sraw + slot * SLOT_BYTES + rr * RAW_ROW;
+          if (qa.general) convert_stage<WQ, true>(rowp, rr, sub, sc, o);
+          else convert_stage<WQ, false>(rowp, rr, sub, sc, o);
+          tmem_st32(a_lane + stage * (BK / 2), o);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&C.full[stage]));
+        } else if (last) {
+          // a slot whose stages are all the other warp's: its release below
+          // must still come after the slot's data arrived (so it counts for
+          // this fill of the buffer, not the previous one)
+          if (!__all_sync(0xffffffffu,
+                          wait_bar(smem_u32(&C.rawfull[slot]), sphase, deadline, abort))) {
+            ok = false;
+            break;
+          }
         }
-        tc_fence_after();
-        uint32_t o[32];
-        const uint32_t rowp = sraw + slot * SLOT_BYTES + rr * RAW_ROW;
-        if (qa.general) convert_stage<WQ, true>(rowp, rr, sub, sc, o);
-        else convert_stage<WQ, false>(rowp, rr, sub, sc, o);
-        tmem_st32(a_lane + stage * (BK / 2), o);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&C.full[stage]));
-        if (sub == SUBS - 1 || kb == kblocks - 1) {  // the slot's last stage read
+        if (last) {
+          __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&C.rawempty[slot]));
           if (++slot == SLOTS) {
             slot = 0;
