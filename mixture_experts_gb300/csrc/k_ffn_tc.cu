@@ -4,29 +4,24 @@
 //
 // For groups of hundreds of rows per expert the FFN is a dense contraction
 // (per expert: rows x d x 2f for gate/up, rows x f x d for down), so it runs
-// on tcgen05: TMA copies 128x64 activation tiles and 256x64 weight tiles
-// (128-byte swizzle) into a 4-stage shared-memory ring, one thread issues
-// tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32 accumulate) into a tensor
-// memory accumulator, and four epilogue warps read the accumulator back with
-// tcgen05.ld. The accumulator is double-buffered in TMEM (2 x 256 of the 512
-// columns) so the epilogue of one tile overlaps the main loop of the next.
+// on tcgen05 with CTA pairs: TMA copies 64-deep slices of the weight tile and
+// the token rows (128-byte swizzle) into a 6-stage shared-memory ring of each
+// CTA, the pair's first CTA issues tcgen05.mma.cta_group::2 (bf16 in, fp32
+// accumulate) into tensor memory, and four epilogue warps per CTA read the
+// accumulator back with tcgen05.ld. The accumulator is double-buffered in
+// tensor memory (2 x 256 of the 512 columns) so the epilogue of one tile
+// overlaps the main loop of the next.
 //
 // Grouping (the per-expert GEMM fed by the token-to-expert map and expert
 // offsets of the trdm.cn overview page, section 3.3): each CTA derives the
 // tile list from the device-side offsets — expert e contributes
-// ceil(rows_e / 128) row tiles x (N / 256) column tiles, experts without rows
-// contribute none (their weights are never read: wzjinhao.cn page,
-// section 2.3) — and walks it with a static stride of gridDim.x, consecutive
-// tiles sharing the weight tile so the L2 serves the other row tiles. Row
-// tiles that run past an expert's rows are computed but not stored (an output
-// row depends on its own input row only, so whatever those rows hold — the
-// next expert's rows, or stale workspace past the last group — never reaches
-// a stored value); rows past the end of the buffer are zero-filled by TMA.
-//
-// Gate/up epilogue: the weights are interleaved in 64-row blocks (gate rows,
-// then the matching up rows), so accumulator columns c and c + 64 of each
-// 128-column half are gate and up of the same feature; h = silu(gate) * up is
-// written as bf16. Down epilogue: fp32 rows of y_perm.
+// ceil(2f or d / 256) weight tiles x ceil(rows_e / 256) token tiles, experts
+// without rows contribute none (their weights are never read: wzjinhao.cn
+// page, section 2.3) — and walks it with a static stride, consecutive tiles
+// sharing the weight tile so the L2 serves the other token tiles. Token
+// columns past an expert's rows are computed but not stored (an output row
+// depends on its own input row only); rows past the end of the buffer are
+// zero-filled by TMA.
 //
 // Every mbarrier wait is bounded by one kernel-wide deadline; a CTA that
 // reaches it latches COLI_ETIMEOUT, unwinds all roles, waits briefly for
@@ -42,293 +37,55 @@ namespace coli {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KiB
 constexpr int TMEM_COLS = 512;
 constexpr int kMaxE = 256;
-constexpr int STAGES = 4;
-constexpr int kThreads = 192;  // warps: 0 TMA, 1 MMA (+ TMEM alloc), 2-5 epilogue
-constexpr int kStageBytes = A_BYTES + B_BYTES;
-
-// bf16 x bf16 -> fp32, A and B K-major, M = 128, N = 256.
-constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
-
-struct __align__(8) Ctrl {
-  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
-  uint32_t tmem_base;
-  int abort;
-  int tile_off[kMaxE + 1];  // first tile of expert e
-  int row_off[kMaxE + 1];   // first row of expert e (the offsets)
-};
-
-constexpr size_t kSmem = 1024 + STAGES * kStageBytes + sizeof(Ctrl);
 
 struct Tile {
-  int e, nt, mt;
+  int e, nt, mt;  // expert, weight tile, token tile
 };
 
-COLI_DEV Tile decode_tile(const Ctrl& C, int E, int n_tiles_n, int t) {
-  int lo = 0, hi = E;  // tile_off[lo] <= t < tile_off[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (C.tile_off[mid] <= t) lo = mid;
-    else hi = mid;
-  }
-  const int rows = C.row_off[lo + 1] - C.row_off[lo];
-  const int mts = (rows + BM - 1) / BM;
-  const int local = t - C.tile_off[lo];
-  return Tile{lo, local / mts, local % mts};
-}
-
-// EPI 0: gate/up + SwiGLU -> bf16 H [rows][N/2]; EPI 1: fp32 out [rows][N];
-// EPI 2: bf16 out [rows][N].
-template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
-    k_tc_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-              const int32_t* __restrict__ offsets, int E, int K, int N, void* __restrict__ out,
-              int* status) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  const uint32_t sa = smem_u32(base);
-  const uint32_t sb = sa + STAGES * A_BYTES;
-  Ctrl& C = *reinterpret_cast<Ctrl*>(base + STAGES * kStageBytes);
-  volatile int* abort = &C.abort;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint64_t deadline = global_timer_ns() + kWaitTimeoutNs;
-  const int n_tiles_n = (N + BN - 1) / BN;
-  const int kblocks = K / BK;
-
-  // tile table from the expert offsets (warp 0), barriers (thread 0),
-  // tensor memory (warp 1)
-  if (warp == 0) {
-    int mts[kMaxE / 32], sum = 0;
-#pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
-      const int e = lane * (kMaxE / 32) + i;
-      int m = 0;
-      if (e < E) {
-        const int r0 = offsets[e], r1 = offsets[e + 1];
-        C.row_off[e] = r0;
-        if (e == E - 1) C.row_off[E] = r1;
-        m = ((r1 - r0 + BM - 1) / BM) * n_tiles_n;
-      }
-      mts[i] = m;
-      sum += m;
-    }
-    int incl = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += y;
-    }
-    int run = incl - sum;
-#pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
-      const int e = lane * (kMaxE / 32) + i;
-      if (e < E) C.tile_off[e] = run;
-      run += mts[i];
-    }
-    if (lane == 31) C.tile_off[E] = incl;  // all tiles
-    if (lane == 0) {
-      for (int s = 0; s < STAGES; ++s) {
-        mbar_init(smem_u32(&C.full[s]), 1);
-        mbar_init(smem_u32(&C.empty[s]), 1);
-      }
-      for (int a = 0; a < 2; ++a) {
-        mbar_init(smem_u32(&C.tfull[a]), 1);
-        mbar_init(smem_u32(&C.tempty[a]), 4);
-      }
-      C.abort = 0;
-      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-  } else if (warp == 1) {
-    tmem_alloc(smem_u32(&C.tmem_base), TMEM_COLS);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = C.tmem_base;
-  const int total = C.tile_off[E];
-
-  if (warp == 0) {
-    if (lane == 0) {  // ---- TMA producer
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
-        const Tile tl = decode_tile(C, E, n_tiles_n, t);
-        const int a_row = C.row_off[tl.e] + tl.mt * BM;
-        const int b_row = tl.e * N + tl.nt * BN;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          // a free slot: the MMA of its last use has completed
-          if (!wait_bar(smem_u32(&C.empty[stage]), phase ^ 1u, deadline, abort)) break;
-          const uint32_t fb = smem_u32(&C.full[stage]);
-          mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-          tma_load_2d(sa + stage * A_BYTES, &map_a, fb, kb * BK, a_row);
-          tma_load_2d(sb + stage * B_BYTES, &map_b, fb, kb * BK, b_row);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {  // ---- MMA issuer
-      int stage = 0, local = 0;
-      uint32_t phase = 0;
-      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x, ++local) {
-        const int acc = local & 1;
-        const uint32_t acc_phase = (local >> 1) & 1;
-        if (!wait_bar(smem_u32(&C.tempty[acc]), acc_phase ^ 1u, deadline, abort)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * BN;
-        bool ok = true;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!wait_bar(smem_u32(&C.full[stage]), phase, deadline, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = sa + stage * A_BYTES, b0 = sb + stage * B_BYTES;
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            umma_ss(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), kIdesc,
-                    (kb | k) != 0 ? 1u : 0u);
-          umma_commit(smem_u32(&C.empty[stage]));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        umma_commit(smem_u32(&C.tfull[acc]));
-      }
-    }
-  } else if (warp < 6) {  // ---- epilogue: warps 2..5, TMEM lanes 32*(warp%4) ..
-    const int qw = warp & 3;
-    const int r = qw * 32 + lane;
-    int local = 0;
-    for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x, ++local) {
-      const int acc = local & 1;
-      const uint32_t acc_phase = (local >> 1) & 1;
-      // warp-uniform verdict: tcgen05.ld below is warp-collective
-      if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&C.tfull[acc]), acc_phase, deadline, abort)))
-        break;
-      tc_fence_after();
-      const Tile tl = decode_tile(C, E, n_tiles_n, t);
-      const int row = C.row_off[tl.e] + tl.mt * BM + r;
-      const bool valid = row < C.row_off[tl.e + 1];
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(qw * 32) << 16) + acc * BN;
-      if constexpr (EPI == 0) {
-        const int F = N / 2;  // features
-        __nv_bfloat16* H = static_cast<__nv_bfloat16*>(out);
-#pragma unroll 1
-        for (int ci = 0; ci < 4; ++ci) {
-          const int c = (ci & 1) + (ci >> 1) * 4;  // gate chunks 0, 1, 4, 5
-          uint32_t g[32], u[32];
-          tmem_ld32(taddr + c * 32, g);
-          tmem_ld32(taddr + (c + 2) * 32, u);
-          const int feat = tl.nt * 128 + (c & 1) * 32 + (c >> 2) * 64;
-          if (valid && feat < F) {
-            uint32_t packed[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float a0 = __uint_as_float(g[2 * j]), a1 = __uint_as_float(g[2 * j + 1]);
-              const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
-              packed[j] = pack_bf16x2(a0 / (1.f + expf(-a0)) * u0, a1 / (1.f + expf(-a1)) * u1);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(H + static_cast<size_t>(row) * F + feat);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                  packed[4 * v + 3]);
-          }
-        }
-      } else if constexpr (EPI == 1) {
-        float* Y = static_cast<float*>(out);
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(taddr + c * 32, v);
-          const int col = tl.nt * BN + c * 32;
-          if (valid && col < N) {
-            uint4* dst = reinterpret_cast<uint4*>(Y + static_cast<size_t>(row) * N + col);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-          }
-        }
-      } else {  // EPI 2: bf16 out (round to nearest even)
-        __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(out);
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(taddr + c * 32, v);
-          const int col = tl.nt * BN + c * 32;
-          if (valid && col < N) {
-            uint32_t p[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              p[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-            uint4* dst = reinterpret_cast<uint4*>(Y + static_cast<size_t>(row) * N + col);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&C.tempty[acc]));
-    }
-  }
-
-  __syncthreads();
-  if (*abort) {
-    if (threadIdx.x == 0) {
-      latch_error(status, kErrTimeout);
-      const uint64_t t0 = global_timer_ns();  // let copies in flight land
-      while (global_timer_ns() - t0 < 1000000ull) {
-      }
-    }
-    __syncthreads();
-  }
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
-  }
-}
-
 // ---- CTA-pair kernel (bf16 weights) ------------------------------------------------
-// A pair of CTAs (a cluster of two, one per SM) computes a 256-row x 256-column
-// tile with cta_group::2 MMAs issued by the first CTA: each CTA loads its own
-// 128 activation rows and half (128 rows) of the weight tile into its shared
-// memory, and the tensor cores of the pair read both halves, so a CTA moves
-// 32 KiB per 64-deep stage instead of 48 KiB for the same MMA work. Each
-// CTA's tensor memory receives its 128 rows of the accumulator and its own
-// four epilogue warps drain them. The first CTA's barriers count the pair's
-// TMA bytes and both CTAs' epilogue arrivals; its MMA commits arrive on the
-// matching barriers of both CTAs.
+// A pair of CTAs (a cluster of two, one per SM) computes a tile of 256 weight
+// rows x up to 256 token rows with cta_group::2 MMAs issued by the first CTA.
+// The weights are the A operand (M = 256: each CTA loads its 128 rows) and
+// the activations the B operand (N = the tile's token rows rounded up to 16:
+// each CTA loads half of them), so a CTA moves 32 KiB per 64-deep stage and
+// an expert's last, partial token tile costs what it holds (with 256-row
+// token tiles the ragged tails were 16-18% extra MMA work on the
+// mixtral_prefill and skewed workloads). Each CTA's tensor memory receives
+// the accumulator rows of its 128 weight rows (D[weight row][token]) and its
+// own four epilogue warps drain them. The first CTA's barriers count the
+// pair's TMA bytes and both CTAs' epilogue arrivals; its MMA commits arrive
+// on the matching barriers of both CTAs.
+//
+// Gate/up: a CTA's 128 weight rows are one interleaved block (gate rows of 64
+// features, then their up rows), so lanes 0-63 hold gate rows and 64-127 the
+// matching up rows. The warps of quarters q and q + 2 pair up: for each
+// 32-token chunk each hands the other half of its values through a small
+// shared-memory buffer (an mbarrier per pair and buffer, bounded waits), the
+// gate warp finishes the chunk's first 16 tokens and the up warp the last 16,
+// and h = silu(gate) * up goes to H [token][feature]. (Loading the weight
+// rows in 16-row boxes so that gate and up of a feature share a warp took
+// eight TMA copies per stage and slowed the gate/up GEMM by 25%.) Down: lane =
+// output column. A store instruction writes 32 consecutive columns of a
+// token row.
 constexpr int PAIR_STAGES = 6;
-constexpr int BH_BYTES = (BN / 2) * BK * 2;  // 16 KiB: a CTA's half of the weight tile
-constexpr uint32_t kIdescPair = idesc_bf16(2 * BM, BN);
+constexpr int WH_BYTES = BM * BK * 2;        // 16 KiB: a CTA's 128 weight rows
+constexpr int XH_BYTES = (BN / 2) * BK * 2;  // 16 KiB: a CTA's half of the 256 token rows
+constexpr int XCH_BYTES = 4 * 2 * 16 * 32 * 4;  // gate/up hand-over: [quarter][buffer][16][32] fp32
 
 struct __align__(8) CtrlPair {
-  uint64_t full[PAIR_STAGES], empty[PAIR_STAGES], tfull[2], tempty[2];
+  uint64_t full[PAIR_STAGES], empty[PAIR_STAGES], tfull[2], tempty[2], xbar[2][2];
   uint32_t tmem_base;
   int abort;
   int tile_off[kMaxE + 1];
   int row_off[kMaxE + 1];
 };
 
-// 16 KiB of headroom after the weight stages: every operand read of the MMAs
-// stays inside this CTA's allocation whatever the stage.
-constexpr int kPairGuard = 16384;
 constexpr size_t kPairSmem =
-    1024 + PAIR_STAGES * (A_BYTES + BH_BYTES) + kPairGuard + sizeof(CtrlPair);
+    1024 + PAIR_STAGES * (WH_BYTES + XH_BYTES) + XCH_BYTES + sizeof(CtrlPair);
 
-// Tile t of the pair grid: expert, 256-column tile, 256-row tile.
+// Tile t of the pair grid: expert, 256-row weight tile, 256-row token tile.
 COLI_DEV Tile decode_pair_tile(const CtrlPair& C, int E, int t) {
   int lo = 0, hi = E;
   while (hi - lo > 1) {
@@ -337,30 +94,37 @@ COLI_DEV Tile decode_pair_tile(const CtrlPair& C, int E, int t) {
     else hi = mid;
   }
   const int rows = C.row_off[lo + 1] - C.row_off[lo];
-  const int mts = (rows + 2 * BM - 1) / (2 * BM);
+  const int mts = (rows + BN - 1) / BN;
   const int local = t - C.tile_off[lo];
   return Tile{lo, local / mts, local % mts};
 }
 
+// Token rows of a tile rounded up to 16 (the MMA's N).
+COLI_DEV int pair_tile_n(const CtrlPair& C, const Tile& tl) {
+  const int rows = min(BN, C.row_off[tl.e + 1] - C.row_off[tl.e] - tl.mt * BN);
+  return (rows + 15) & ~15;
+}
+
 template <int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
-    k_tc_gemm_pair(const __grid_constant__ CUtensorMap map_a,
-                   const __grid_constant__ CUtensorMap map_b, const int32_t* __restrict__ offsets,
+    k_tc_gemm_pair(const __grid_constant__ CUtensorMap map_x,
+                   const __grid_constant__ CUtensorMap map_w, const int32_t* __restrict__ offsets,
                    int E, int K, int N, void* __restrict__ out, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const uint32_t sa = smem_u32(base);
-  const uint32_t sb = sa + PAIR_STAGES * A_BYTES;
+  const uint32_t sw = smem_u32(base);                // weight stages (A)
+  const uint32_t sx = sw + PAIR_STAGES * WH_BYTES;  // activation stages (B)
+  float* xch = reinterpret_cast<float*>(base + PAIR_STAGES * (WH_BYTES + XH_BYTES));
   CtrlPair& C =
-      *reinterpret_cast<CtrlPair*>(base + PAIR_STAGES * (A_BYTES + BH_BYTES) + kPairGuard);
+      *reinterpret_cast<CtrlPair*>(base + PAIR_STAGES * (WH_BYTES + XH_BYTES) + XCH_BYTES);
   volatile int* abort = &C.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const bool first = rank == 0;
   const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
   const uint64_t deadline = global_timer_ns() + kWaitTimeoutNs;
-  const int n_tiles_n = (N + BN - 1) / BN;
+  const int n_wt = (N + BN - 1) / BN;  // 256-row weight tiles per expert
   const int kblocks = K / BK;
 
   if (warp == 0) {
@@ -373,7 +137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const int r0 = offsets[e], r1 = offsets[e + 1];
         C.row_off[e] = r0;
         if (e == E - 1) C.row_off[E] = r1;
-        m = ((r1 - r0 + 2 * BM - 1) / (2 * BM)) * n_tiles_n;
+        m = ((r1 - r0 + BN - 1) / BN) * n_wt;
       }
       mts[i] = m;
       sum += m;
@@ -400,6 +164,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       for (int a = 0; a < 2; ++a) {
         mbar_init(smem_u32(&C.tfull[a]), 1);
         mbar_init(smem_u32(&C.tempty[a]), 8);  // four epilogue warps in each CTA
+        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&C.xbar[a][b]), 2);  // a warp pair
       }
       C.abort = 0;
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -415,20 +180,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   const int total = C.tile_off[E];
 
   if (warp == 0) {
-    if (lane == 0) {  // ---- TMA producer (both CTAs): own rows, own half of B
+    if (lane == 0) {  // ---- TMA producer (both CTAs): own weight rows, own half of the tokens
       int stage = 0;
       uint32_t phase = 0;
       for (int t = pair; t < total && !*abort; t += n_pairs) {
         const Tile tl = decode_pair_tile(C, E, t);
-        const int a_row = C.row_off[tl.e] + tl.mt * 2 * BM + static_cast<int>(rank) * BM;
-        const int b_row = tl.e * N + tl.nt * BN + static_cast<int>(rank) * (BN / 2);
+        const int w_row = tl.e * N + tl.nt * BN + static_cast<int>(rank) * BM;
+        const int x_row = C.row_off[tl.e] + tl.mt * BN +
+                          static_cast<int>(rank) * (pair_tile_n(C, tl) / 2);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar_cluster(smem_u32(&C.empty[stage]), phase ^ 1u, deadline, abort)) break;
           const uint32_t fb = smem_u32(&C.full[stage]);
-          if (first) mbar_arrive_expect_tx(fb, 2 * (A_BYTES + BH_BYTES));
+          if (first) mbar_arrive_expect_tx(fb, 2 * (WH_BYTES + XH_BYTES));
           const uint32_t fb0 = map_shared(fb, 0);
-          tma_load_2d_pair(sa + stage * A_BYTES, &map_a, fb0, kb * BK, a_row);
-          tma_load_2d_pair(sb + stage * BH_BYTES, &map_b, fb0, kb * BK, b_row);
+          tma_load_2d_pair(sw + stage * WH_BYTES, &map_w, fb0, kb * BK, w_row);
+          tma_load_2d_pair(sx + stage * XH_BYTES, &map_x, fb0, kb * BK, x_row);
           if (++stage == PAIR_STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -446,6 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         if (!wait_bar_cluster(smem_u32(&C.tempty[acc]), acc_phase ^ 1u, deadline, abort)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * BN;
+        const uint32_t idesc = idesc_bf16(2 * BM, pair_tile_n(C, decode_pair_tile(C, E, t)));
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!wait_bar_cluster(smem_u32(&C.full[stage]), phase, deadline, abort)) {
@@ -453,10 +220,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = sa + stage * A_BYTES, b0 = sb + stage * BH_BYTES;
+          const uint32_t a0 = sw + stage * WH_BYTES, b0 = sx + stage * XH_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            umma_ss_pair(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), kIdescPair,
+            umma_ss_pair(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc,
                          (kb | k) != 0 ? 1u : 0u);
           umma_commit_pair(smem_u32(&C.empty[stage]));
           if (++stage == PAIR_STAGES) {
@@ -468,10 +235,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         umma_commit_pair(smem_u32(&C.tfull[acc]));
       }
     }
-  } else {  // ---- epilogue (both CTAs): warps 2..5, this CTA's 128 rows
-    const int qw = warp & 3;
-    const int r = qw * 32 + lane;
+  } else {  // ---- epilogue (both CTAs): warps 2..5, lanes 32*(warp%4) .. of this CTA's rows
+    const int q = warp & 3;
     int local = 0;
+    uint32_t xseq = 0;   // gate/up hand-overs so far (the pair's buffers alternate)
+    bool xfail = false;  // a hand-over wait gave up
     for (int t = pair; t < total && !*abort; t += n_pairs, ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
@@ -480,64 +248,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         break;
       tc_fence_after();
       const Tile tl = decode_pair_tile(C, E, t);
-      const int row = C.row_off[tl.e] + tl.mt * 2 * BM + static_cast<int>(rank) * BM + r;
-      const bool valid = row < C.row_off[tl.e + 1];
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(qw * 32) << 16) + acc * BN;
+      const int tok0 = C.row_off[tl.e] + tl.mt * BN;
+      const int tok_end = C.row_off[tl.e + 1];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + acc * BN;
       if constexpr (EPI == 0) {
         const int F = N / 2;
         __nv_bfloat16* H = static_cast<__nv_bfloat16*>(out);
+        const bool up = q >= 2;
+        const int pq = q & 1;  // pair: gate quarter pq, up quarter pq + 2
+        const int blk = 2 * tl.nt + static_cast<int>(rank);
+        const int feat = blk * 64 + 32 * pq + lane;
+        if (blk * 64 < F) {  // this CTA's block lies inside the expert's rows
 #pragma unroll 1
-        for (int ci = 0; ci < 4; ++ci) {
-          const int c = (ci & 1) + (ci >> 1) * 4;
-          uint32_t g[32], u[32];
-          tmem_ld32(taddr + c * 32, g);
-          tmem_ld32(taddr + (c + 2) * 32, u);
-          const int feat = tl.nt * 128 + (c & 1) * 32 + (c >> 2) * 64;
-          if (valid && feat < F) {
-            uint32_t packed[16];
+          for (int c = 0; c < BN / 32; ++c) {
+            const int t0 = tok0 + 32 * c;
+            if (t0 >= tok_end) break;
+            uint32_t v[32];
+            tmem_ld32(taddr + 32 * c, v);
+            // hand the partner what it finishes: the gate warp's values of
+            // tokens 16..31, the up warp's of tokens 0..15
+            const int b = xseq & 1;
+            const uint32_t xph = (xseq >> 1) & 1u;
+            ++xseq;
+            float* mine = xch + ((q * 2 + b) * 16) * 32;
+            const float* theirs = xch + (((q ^ 2) * 2 + b) * 16) * 32;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) mine[j * 32 + lane] = __uint_as_float(v[up ? j : 16 + j]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&C.xbar[pq][b]));
+            if (!__all_sync(0xffffffffu,
+                            wait_bar(smem_u32(&C.xbar[pq][b]), xph, deadline, abort))) {
+              xfail = true;
+              break;
+            }
+            // (silu with the fast exponential and division: h is rounded to
+            // bf16, far coarser than their few-ulp error)
+            const int tb = t0 + (up ? 16 : 0);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const float a0 = __uint_as_float(g[2 * j]), a1 = __uint_as_float(g[2 * j + 1]);
-              const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
-              packed[j] = pack_bf16x2(a0 / (1.f + expf(-a0)) * u0, a1 / (1.f + expf(-a1)) * u1);
+              const float other = theirs[j * 32 + lane];
+              const float g = up ? other : __uint_as_float(v[j]);
+              const float u = up ? __uint_as_float(v[16 + j]) : other;
+              if (tb + j < tok_end)
+                H[static_cast<size_t>(tb + j) * F + feat] =
+                    __float2bfloat16_rn(__fdividef(g, 1.f + __expf(-g)) * u);
             }
-            uint4* dst = reinterpret_cast<uint4*>(H + static_cast<size_t>(row) * F + feat);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                  packed[4 * v + 3]);
           }
-        }
-      } else if constexpr (EPI == 1) {
-        float* Y = static_cast<float*>(out);
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(taddr + c * 32, v);
-          const int col = tl.nt * BN + c * 32;
-          if (valid && col < N) {
-            uint4* dst = reinterpret_cast<uint4*>(Y + static_cast<size_t>(row) * N + col);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-          }
+          if (xfail) break;
         }
       } else {
-        __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(out);
+        const int col = tl.nt * BN + static_cast<int>(rank) * BM + 32 * q + lane;
+        if (col - lane < N) {  // this warp's 32 columns lie inside the output
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(taddr + c * 32, v);
-          const int col = tl.nt * BN + c * 32;
-          if (valid && col < N) {
-            uint32_t pk[16];
+          for (int c = 0; c < BN / 32; ++c) {
+            const int t0 = tok0 + 32 * c;
+            if (t0 >= tok_end) break;
+            uint32_t v[32];
+            tmem_ld32(taddr + 32 * c, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-            uint4* dst = reinterpret_cast<uint4*>(Y + static_cast<size_t>(row) * N + col);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            for (int j = 0; j < 32; ++j) {
+              if (t0 + j >= tok_end) break;
+              const size_t at = static_cast<size_t>(t0 + j) * N + col;
+              if constexpr (EPI == 1) static_cast<float*>(out)[at] = __uint_as_float(v[j]);
+              else
+                static_cast<__nv_bfloat16*>(out)[at] =
+                    __float2bfloat16_rn(__uint_as_float(v[j]));
+            }
           }
         }
       }
@@ -602,21 +378,18 @@ cudaError_t encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_byte
 
 struct TcPlan {
   CUtensorMap map_wgu, map_wdn, map_xperm, map_h;
-  bool pair;           // CTA-pair kernel with half-height weight maps
   QPlan* q = nullptr;  // int4 / MX weights: the tensor-memory-operand kernel
   int E, d, f, grid;
 };
 
 bool tc_supported(int wdt, int d, int f) {
   if (encode_fn() == nullptr) return false;
-  if (wdt == DT_BF16) return d % 64 == 0 && f % 64 == 0;
-  return tcq_supported(wdt, d, f);
-}
-
-template <int EPI>
-static cudaError_t set_smem() {
-  return cudaFuncSetAttribute(k_tc_gemm<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kSmem));
+  if (wdt != DT_BF16) return tcq_supported(wdt, d, f);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return false;
+  return d % 64 == 0 && f % 64 == 0 && sms >= 2;  // CTA pairs
 }
 
 cudaError_t tc_plan_create(TcPlan** plan, int wdt, const void* w_gu, const void* w_dn,
@@ -644,21 +417,17 @@ cudaError_t tc_plan_create(TcPlan** plan, int wdt, const void* w_gu, const void*
     delete p;
     return e;
   }
-  // each CTA of a pair loads 128 of the 256 weight rows of a tile
-  p->pair = sms >= 2;
-  p->grid = p->pair ? sms & ~1 : sms;  // whole pairs
-  const int box = p->pair ? BN / 2 : BN;
-  e = make_map(&p->map_wgu, w_gu, static_cast<uint64_t>(E) * 2 * f, d, box);
-  if (e == cudaSuccess) e = make_map(&p->map_wdn, w_dn, static_cast<uint64_t>(E) * d, f, box);
-  if (e == cudaSuccess) e = set_smem<0>();
-  if (e == cudaSuccess) e = set_smem<1>();
-  if (e == cudaSuccess) e = set_smem<2>();
+  p->grid = sms & ~1;  // whole pairs
+  // a CTA's 128 weight rows; token rows in a CTA's half of 256
+  e = make_map(&p->map_wgu, w_gu, static_cast<uint64_t>(E) * 2 * f, d, BM);
+  if (e == cudaSuccess) e = make_map(&p->map_wdn, w_dn, static_cast<uint64_t>(E) * d, f, BM);
   for (auto fn : {k_tc_gemm_pair<0>, k_tc_gemm_pair<1>, k_tc_gemm_pair<2>})
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(kPairSmem));
-  if (e == cudaSuccess) e = make_map(&p->map_xperm, x_perm, static_cast<uint64_t>(max_rows), d, BM);
-  if (e == cudaSuccess) e = make_map(&p->map_h, H, static_cast<uint64_t>(max_rows), f, BM);
+  if (e == cudaSuccess)
+    e = make_map(&p->map_xperm, x_perm, static_cast<uint64_t>(max_rows), d, BN / 2);
+  if (e == cudaSuccess) e = make_map(&p->map_h, H, static_cast<uint64_t>(max_rows), f, BN / 2);
   if (e != cudaSuccess) {
     delete p;
     return e;
@@ -673,15 +442,11 @@ void tc_plan_destroy(TcPlan* plan) {
 }
 
 template <int EPI>
-static void launch(const TcPlan* p, const CUtensorMap& map_a, const CUtensorMap& map_b,
+static void launch(const TcPlan* p, const CUtensorMap& map_x, const CUtensorMap& map_w,
                    const int32_t* offsets, int K, int N, void* out, cudaStream_t st,
                    int* status) {
-  if (p->pair)
-    k_tc_gemm_pair<EPI><<<p->grid, 192, kPairSmem, st>>>(map_a, map_b, offsets, p->E, K, N, out,
-                                                         status);
-  else
-    k_tc_gemm<EPI><<<p->grid, kThreads, kSmem, st>>>(map_a, map_b, offsets, p->E, K, N, out,
-                                                     status);
+  k_tc_gemm_pair<EPI><<<p->grid, 192, kPairSmem, st>>>(map_x, map_w, offsets, p->E, K, N, out,
+                                                       status);
 }
 
 cudaError_t launch_tc_gateup(TcPlan* p, const void* x_perm, bool own_x_perm,
@@ -689,14 +454,14 @@ cudaError_t launch_tc_gateup(TcPlan* p, const void* x_perm, bool own_x_perm,
                              int* status) {
   if (p->q) return launch_tcq_gateup(p->q, x_perm, own_x_perm, offsets, H, n_rows, st, status);
   if (n_rows == 0) return cudaSuccess;
-  CUtensorMap map_a;
+  CUtensorMap map_x;
   if (own_x_perm) {
-    map_a = p->map_xperm;
+    map_x = p->map_xperm;
   } else {
-    const cudaError_t e = make_map(&map_a, x_perm, static_cast<uint64_t>(n_rows), p->d, BM);
+    const cudaError_t e = make_map(&map_x, x_perm, static_cast<uint64_t>(n_rows), p->d, BN / 2);
     if (e != cudaSuccess) return e;
   }
-  launch<0>(p, map_a, p->map_wgu, offsets, p->d, 2 * p->f, H, st, status);
+  launch<0>(p, map_x, p->map_wgu, offsets, p->d, 2 * p->f, H, st, status);
   return cudaGetLastError();
 }
 
