@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
 
 namespace coli {
 namespace {
@@ -658,6 +659,213 @@ __global__ void __launch_bounds__(256, 1)
 #undef COLI_SELECT_BIG
 }
 
+// ---- bf16, many tokens, 32 < E <= 128: tensor cores with tensor memory ----------------
+// A CTA takes 128 tokens (the MMA's M, one tensor-memory lane each) and all E
+// experts (N = E rounded up to 16). TMA brings 64-index chunks of the token
+// rows and of W_r (128-byte swizzle) into a 6-stage ring, so a CTA keeps up
+// to 144 KiB of loads in flight and one wave of CTAs streams x at HBM speed.
+// One thread issues tcgen05.mma; every chunk goes into a fresh accumulator
+// (one of four tensor-memory buffers), and the thread of each token adds the
+// chunk's E partial sums into its fp32 running logits in chunk order, so the
+// tensor core never carries a sum across more than 64 products. That thread
+// then adds the bias and selects the token's top-k from its registers (k+1
+// rounds of arg-max: larger value, then lower index), with the gates and the
+// k-th/(k+1)-th gap as in select_token.
+constexpr int kGTok = 128;    // tokens per CTA
+constexpr int kGK = 64;       // reduction indices per chunk
+constexpr int kGStages = 6;
+constexpr int kGBufs = 4;     // tensor-memory partial buffers
+constexpr int kGThreads = 192;  // warps: 0 TMA, 1 MMA, 2-5 tokens
+
+template <int EMAX>
+constexpr size_t g_smem_bytes() {
+  return 1024 + kGStages * (kGTok * kGK * 2 + EMAX * kGK * 2) + 256;
+}
+
+struct __align__(8) GCtrl {
+  uint64_t full[kGStages], empty[kGStages], dfull[kGBufs], dempty[kGBufs];
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int EMAX>
+__global__ void __launch_bounds__(kGThreads, 1)
+    k_route_tcg(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                const float* __restrict__ b, int T, int d, int E, int k,
+                int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                float* __restrict__ gap, int* status) {
+  constexpr int XB = kGTok * kGK * 2, WB = EMAX * kGK * 2;
+  constexpr uint32_t kCols = kGBufs * EMAX;  // 256 or 512 tensor-memory columns
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sx = smem_u32(base), sw = sx + kGStages * XB;
+  GCtrl& C = *reinterpret_cast<GCtrl*>(base + kGStages * (XB + WB));
+  volatile int* abort = &C.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t deadline = global_timer_ns() + kWaitTimeoutNs;
+  const int t0 = blockIdx.x * kGTok;
+  const int Ep = (E + 15) & ~15;
+  const int chunks = d / kGK;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < kGStages; ++s) {
+      mbar_init(smem_u32(&C.full[s]), 1);
+      mbar_init(smem_u32(&C.empty[s]), 1);
+    }
+    for (int s = 0; s < kGBufs; ++s) {
+      mbar_init(smem_u32(&C.dfull[s]), 1);
+      mbar_init(smem_u32(&C.dempty[s]), 4);
+    }
+    C.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  } else if (warp == 1) {
+    tmem_alloc(smem_u32(&C.tmem_base), kCols);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = C.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer
+      const uint32_t bytes = XB + static_cast<uint32_t>(Ep) * kGK * 2;
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int c = 0; c < chunks; ++c) {
+        if (!wait_bar(smem_u32(&C.empty[stage]), phase ^ 1u, deadline, abort)) break;
+        const uint32_t fb = smem_u32(&C.full[stage]);
+        mbar_arrive_expect_tx(fb, bytes);
+        tma_load_2d(sx + stage * XB, &map_x, fb, c * kGK, t0);
+        tma_load_2d(sw + stage * WB, &map_w, fb, c * kGK, 0);
+        if (++stage == kGStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA issuer: one fresh accumulator per chunk
+      const uint32_t idesc = idesc_bf16(kGTok, Ep);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int c = 0; c < chunks; ++c) {
+        const int buf = c % kGBufs;
+        if (!wait_bar(smem_u32(&C.dempty[buf]), ((c / kGBufs) & 1) ^ 1u, deadline, abort)) break;
+        if (!wait_bar(smem_u32(&C.full[stage]), phase, deadline, abort)) break;
+        tc_fence_after();
+        const uint32_t a0 = sx + stage * XB, b0 = sw + stage * WB;
+#pragma unroll
+        for (int kk = 0; kk < kGK / 16; ++kk)
+          umma_ss(tmem + buf * EMAX, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                  kk != 0 ? 1u : 0u);
+        umma_commit(smem_u32(&C.empty[stage]));
+        umma_commit(smem_u32(&C.dfull[buf]));
+        if (++stage == kGStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else {  // ---- tokens: warps 2..5, lane 32*(warp%4) + lane = token t0 + that
+    const int q = warp & 3;
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    float acc[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
+    bool ok = true;
+    for (int c = 0; c < chunks; ++c) {
+      const int buf = c % kGBufs;
+      // warp-uniform verdict: tcgen05.ld below is warp-collective
+      if (!__all_sync(0xffffffffu, wait_bar(smem_u32(&C.dfull[buf]), (c / kGBufs) & 1,
+                                            deadline, abort))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < EMAX / 32; ++cc) {
+        if (32 * cc < Ep) {
+          uint32_t v[32];
+          tmem_ld32(tlane + buf * EMAX + 32 * cc, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[32 * cc + i] += __uint_as_float(v[i]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&C.dempty[buf]));
+    }
+    const int t = t0 + 32 * q + lane;
+    if (ok && t < T) {
+      uint32_t key[EMAX];
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e)
+        key[e] = e < E ? order_key(rankable(acc[e] + (b != nullptr ? b[e] : 0.f), status)) : 0u;
+      float sel_val[8];
+      int sel_idx[8];
+      float kth = 0.f, next = INFINITY;  // l_(k) and l_(k+1)
+      const int rounds = min(k + 1, E);
+#pragma unroll
+      for (int r = 0; r < 9; ++r) {
+        if (r < 8) {
+          sel_val[r] = -INFINITY;
+          sel_idx[r] = 0;
+        }
+        if (r < rounds) {
+          uint32_t best = 0u;
+          int bi = 0;
+#pragma unroll
+          for (int e = 0; e < EMAX; ++e)
+            if (key[e] > best) {  // strictly greater: the lower index wins ties
+              best = key[e];
+              bi = e;
+            }
+#pragma unroll
+          for (int e = 0; e < EMAX; ++e)
+            if (e == bi) key[e] = 0u;  // taken
+          const float v = key_value(best);
+          if (r < 8) {
+            sel_val[r] = v;
+            sel_idx[r] = bi;
+          }
+          if (r == k - 1) kth = v;
+          if (r == k) next = v;
+        }
+      }
+      if (gap != nullptr) gap[t] = (k < E) ? kth - next : INFINITY;
+      float ex[8], den = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < k) {
+          ex[j] = expf(sel_val[j] - sel_val[0]);
+          den += ex[j];
+        }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < k) {
+          topk_idx[static_cast<size_t>(t) * k + j] = sel_idx[j];
+          topk_w[static_cast<size_t>(t) * k + j] = ex[j] / den;
+        }
+    }
+  }
+
+  __syncthreads();
+  if (*abort) {
+    if (threadIdx.x == 0) {
+      latch_error(status, kErrTimeout);
+      const uint64_t s0 = global_timer_ns();  // let copies in flight land
+      while (global_timer_ns() - s0 < 1000000ull) {
+      }
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
 int slices_for(int d) { return (d + kKS - 1) / kKS; }
 
 }  // namespace
@@ -676,6 +884,40 @@ cudaError_t launch_route(const void* x, const void* w_r, const float* b_r, int T
   if (T == 0) return cudaSuccess;
   const dim3 block(kWarps * 32);
   const dim3 grid((T + kWarps - 1) / kWarps);
+  if (act == DT_BF16 && T >= kTiledMinTokens && E > 32 && E <= 128 && E % 16 == 0) {
+    // many tokens, up to 128 experts: one launch on the 5th-generation tensor cores
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static bool attr_set[2][128] = {};  // per kernel and device: more than 48 KiB of smem
+    CUtensorMap mx, mw;
+    cudaError_t e = encode_tmap_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, T, d, kGK, kGTok,
+                                   CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e == cudaSuccess)
+      e = encode_tmap_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_r, E, d, kGK, E,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+    const int which = E <= 64 ? 0 : 1;
+    const size_t smem = which == 0 ? g_smem_bytes<64>() : g_smem_bytes<128>();
+    if (dev >= 0 && dev < 128 && !attr_set[which][dev]) {
+      e = which == 0 ? cudaFuncSetAttribute(k_route_tcg<64>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(smem))
+                     : cudaFuncSetAttribute(k_route_tcg<128>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      attr_set[which][dev] = true;
+    }
+    const unsigned grid_t = static_cast<unsigned>((T + kGTok - 1) / kGTok);
+    if (which == 0)
+      k_route_tcg<64><<<grid_t, kGThreads, smem, st>>>(mx, mw, b_r, T, d, E, k, topk_idx,
+                                                       topk_w, gap, status);
+    else
+      k_route_tcg<128><<<grid_t, kGThreads, smem, st>>>(mx, mw, b_r, T, d, E, k, topk_idx,
+                                                        topk_w, gap, status);
+    if (n_launches) *n_launches += 1;
+    return cudaGetLastError();
+  }
   if (act == DT_BF16 && T >= kTiledMinTokens && E > 32) {
     // many tokens, many experts: one launch, 64 tokens per block, pipelined
     int dev = 0;

@@ -75,13 +75,14 @@ def test_combine_after_skipped_ids_reads_nothing_out_of_range():
     assert moe.coli_device_status() == moe.COLI_OK
 
 
-@pytest.mark.parametrize("E,k", [(8, 2), (64, 4)])
-def test_nan_router_row_still_gives_k_distinct_ids(E, k):
+@pytest.mark.parametrize("E,k,T", [(8, 2, 20), (64, 4, 20), (64, 4, 1100), (40, 3, 1100)])
+def test_nan_router_row_still_gives_k_distinct_ids(E, k, T):
     """A NaN in a token's activations makes its logits NaN: the router ranks
     them as -inf, so the token still gets k distinct ids in [0, E), and the
-    data error is latched (both the fused E <= 32 and the E > 32 router)."""
+    data error is latched (the fused E <= 32 router, the two-launch E > 32
+    router, and the one-launch tensor-core routers of 1024+ tokens)."""
     assert moe.coli_device_status() == moe.COLI_OK
-    T, d = 20, 256
+    d = 256
     s = inputs.MoEShape("nan", T=T, d=d, E=E, k=k, f=64)
     lay = inputs.make_layer(s, seed=8, experts=False)
     x = lay["x"].clone()

@@ -180,14 +180,20 @@ def test_stage_route_topk(E, k, act, bias):
     assert np.max(np.abs(g[fin] - r_gap[fin]), initial=0.0) <= 3e-6
 
 
-@pytest.mark.parametrize("E,k,bias", [(3, 1, False), (8, 2, True), (24, 3, False), (40, 5, True),
-                                      (64, 4, True), (200, 7, False), (256, 8, False)])
-def test_stage_route_topk_many_tokens(E, k, bias):
-    """bf16 batches of 1024+ tokens take the one-launch router (32 tokens per
-    block, tensor-core logits, the reduction split over warps when E is small):
-    expert counts that fill one, some or all of the block's warps, a ragged
-    last block, with and without bias."""
-    T, d = 1100, 384
+@pytest.mark.parametrize("E,k,bias,d", [(3, 1, False, 384), (8, 2, True, 384),
+                                        (24, 3, False, 384), (40, 5, True, 384),
+                                        (48, 3, True, 384), (64, 4, True, 384),
+                                        (64, 4, True, 2048), (96, 2, False, 384),
+                                        (112, 6, True, 384), (128, 8, False, 768),
+                                        (200, 7, False, 384), (256, 8, False, 384)])
+def test_stage_route_topk_many_tokens(E, k, bias, d):
+    """bf16 batches of 1024+ tokens take a one-launch router: E <= 32, 32
+    tokens per block with mma.sync logits; E a multiple of 16 up to 128, 128
+    tokens per CTA with tcgen05 logits in tensor memory (d = 2048 wraps its
+    stage ring and accumulator buffers many times); other E, 64 tokens per
+    block with mma.sync. Expert counts that fill one, some or all of a block's
+    warps, a ragged last block, with and without bias."""
+    T = 1100
     s = S("route_many", T=T, d=d, E=E, k=k, f=64, bias="zipf" if bias else "none")
     lay, dev = _stage_layer(s, 22)
     idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
