@@ -457,37 +457,46 @@ def measure(s, steps, warmup, world, rank, local, cpu_seconds, with_e2e=True,
     pre = busy(0.5)
     barrier()
 
-    # ---- timed region: K forwards with stage timing on the launching stream
-    moe.coli_moe_set_timing(layer.h, True)
-    moe.coli_moe_stage_times(layer.h)  # reset sums
-    barrier()
-    if flush:
-        per = []
-        for _ in range(steps):
-            scrub.zero_()
+    def timed_pass() -> float:
+        """K forwards between CUDA events on the launching stream (L2 flushed
+        before each one when the inputs fit in L2); returns milliseconds."""
+        barrier()
+        if flush:
+            per = []
+            for _ in range(steps):
+                scrub.zero_()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                layer(x, y)
+                b.record(stream)
+                b.synchronize()
+                per.append(a.elapsed_time(b))
+            ms = sum(per)
+        else:
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            layer(x, y)
+            for _ in range(steps):
+                layer(x, y)
             b.record(stream)
-            b.synchronize()
-            per.append(a.elapsed_time(b))
-        elapsed_ms = sum(per)
-    else:
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(steps):
-            layer(x, y)
-        b.record(stream)
+            barrier()
+            ms = a.elapsed_time(b)
         barrier()
-        elapsed_ms = a.elapsed_time(b)
-    barrier()
+        return ms
+
+    # ---- timed region: K forwards, no instrumentation inside
+    elapsed_ms = timed_pass()
+    # ---- the same K forwards again with per-stage CUDA events, for the split
+    moe.coli_moe_set_timing(layer.h, True)
+    moe.coli_moe_stage_times(layer.h)  # reset sums
+    timed_pass()
     stage_ms, n_fwd, n_launch = moe.coli_moe_stage_times(layer.h)
     moe.coli_moe_set_timing(layer.h, False)
     post = busy(0.5 - elapsed_ms / 1e3) if elapsed_ms < 500.0 else 0
     clk = clocks.stop()
-    clk["window"] = (f"{pre} untimed forwards while the sampler started, the timed region"
+    clk["window"] = (f"{pre} untimed forwards while the sampler started, the timed region, "
+                     "the same forwards again with per-stage events"
                      + (f", then {post} more untimed forwards (the timed region lasted "
                         f"{elapsed_ms:.1f} ms)" if post else ""))
     tokens, seconds = aggregate(s.T * steps, elapsed_ms / 1e3, world)
