@@ -91,3 +91,64 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--config", "tiny_fp32", "--steps", "1", "--warmup", "0"],
                        capture_output=True, text=True, timeout=120, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_roofline_decode_arithmetic():
+    """The decode line's roofline: achieved = gate/up weight bytes of the
+    activated experts / the gate/up stage time, frac = achieved / peak; the
+    whole-FFN and whole-layer figures use all three projections."""
+    import bench
+    from mixture_experts_gb300 import inputs
+    s = inputs.CONFIGS["mixtral_decode"]
+    pk = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0}
+    avg = [0.01, 0.01, 0.300, 0.150, 0.01]  # ms per stage
+    r = bench.roofline(s, "decode", s.T * s.k, 8, avg, 0.5, pk, "measured", "no_such_config")
+    per_expert = 2 * s.f * s.d * 2
+    assert r["bound"] == "hbm" and r["algorithmic_bytes_per_launch"] == 8 * per_expert
+    assert r["achieved"] == pytest.approx(8 * per_expert / 0.300e-3 / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6000.0)
+    all_bytes = 8 * 3 * s.f * s.d * 2
+    assert r["expert_ffn_total"]["bytes"] == all_bytes
+    assert r["layer"]["achieved_gbs"] == pytest.approx(all_bytes / 0.5e-3 / 1e9)
+    assert r["traffic"] is None  # no committed capture under that name
+
+
+def test_roofline_prefill_arithmetic():
+    """The prefill line's roofline: gate/up FLOP (2 x rows x d x 2f) over the
+    gate/up stage time against the sustained and the burst bf16 peaks, the
+    down GEMM and the whole layer (2 x rows x 3 x d x f FLOP) beside it."""
+    import bench
+    from mixture_experts_gb300 import inputs
+    s = inputs.CONFIGS["mixtral_prefill"]
+    pk = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1800.0}
+    rows = s.T * s.k
+    avg = [0.02, 0.03, 1.300, 0.650, 0.03]
+    r = bench.roofline(s, "prefill", rows, 8, avg, 2.0, pk, "measured", "no_such_config")
+    fl = 2.0 * rows * s.d * 2 * s.f
+    assert r["bound"] == "tensor" and r["algorithmic_flops_per_launch"] == fl
+    assert r["achieved"] == pytest.approx(fl / 1.300e-3 / 1e12)
+    assert r["frac_burst"] == pytest.approx(r["achieved"] / 2000.0)
+    assert r["frac"] == r["frac_sustained"] == pytest.approx(r["achieved"] / 1800.0)
+    assert r["down_gemm"]["achieved"] == pytest.approx(2.0 * rows * s.f * s.d / 0.650e-3 / 1e12)
+    assert r["layer"]["flops"] == 2.0 * rows * 3 * s.d * s.f
+    # bf16 activations: the prefill forward writes y_perm in bf16
+    assert r["overhead_bytes"]["y_perm"] == 2 * rows * s.d * 2
+
+
+def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
+    """A committed DRAM-traffic figure is reported only while the hash of the
+    kernel's sources matches the one recorded with it."""
+    import bench
+    real = bench.sources_sha("dec")  # the hash of the sources in this tree
+    rec = {"mixtral_decode": {"kernel": "k_dec_gateup", "bytes_per_launch": 123,
+                              "source_sha": real, "how": "test"},
+           "mixtral_prefill": {"kernel": "k_tc_gemm_pair<0>", "bytes_per_launch": 456,
+                               "source_sha": "0" * 16, "how": "test"}}
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    # the kernel files stay where they are; only the record is the test's
+    monkeypatch.setattr(bench, "sources_sha", lambda kind: real if kind == "dec" else "f" * 16)
+    assert bench.traffic_record("mixtral_decode", "dec") == 123
+    assert bench.traffic_record("mixtral_prefill", "tc") is None  # sources changed
+    assert bench.traffic_record("skewed", "tc") is None  # never captured
