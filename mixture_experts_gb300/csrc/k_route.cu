@@ -344,22 +344,36 @@ COLI_DEV void select_token(const float (&l)[PER_LANE], int E, int k, int t,
   }
 }
 
+// Blocks of kSelWarps warps, one token per warp: a few hundred tokens still
+// spread over most SMs. Each expert's logit is the slice sum in slice order;
+// the slices are the outer loop, so a lane has its PER_LANE loads of a slice
+// in flight together.
+constexpr int kSelWarps = 2;
+
 template <int PER_LANE>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kSelWarps * 32)
     k_route_select(const float* __restrict__ part, int slices, const float* __restrict__ b,
                    int T, int E, int k, int32_t* __restrict__ topk_idx,
                    float* __restrict__ topk_w, float* __restrict__ gap, int* status) {
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int t = blockIdx.x * kSelWarps + (threadIdx.x >> 5);
   if (t >= T) return;
   float l[PER_LANE];
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) l[i] = 0.f;
+  const float* row = part + static_cast<size_t>(t) * E + lane;
+  for (int s = 0; s < slices; ++s) {
+    const float* ps = row + static_cast<size_t>(s) * T * E;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i)
+      if (lane + 32 * i < E) l[i] += ps[32 * i];
+  }
 #pragma unroll
   for (int i = 0; i < PER_LANE; ++i) {
     const int e = lane + 32 * i;
     float v = -INFINITY;
     if (e < E) {
-      v = 0.f;
-      for (int s = 0; s < slices; ++s) v += part[(static_cast<size_t>(s) * T + t) * E + e];
+      v = l[i];
       if (b != nullptr) v += b[e];
       v = rankable(v, status);
     }
@@ -992,15 +1006,16 @@ cudaError_t launch_route(const void* x, const void* w_r, const float* b_r, int T
                                                static_cast<const __nv_bfloat16*>(w_r), T, d, E,
                                                part);
   }
+  const dim3 sblock(kSelWarps * 32), sgrid((T + kSelWarps - 1) / kSelWarps);
   if (E <= 64)
-    k_route_select<2><<<grid, block, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap,
-                                              status);
+    k_route_select<2><<<sgrid, sblock, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap,
+                                                status);
   else if (E <= 128)
-    k_route_select<4><<<grid, block, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap,
-                                              status);
+    k_route_select<4><<<sgrid, sblock, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap,
+                                                status);
   else
-    k_route_select<8><<<grid, block, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap,
-                                              status);
+    k_route_select<8><<<sgrid, sblock, 0, st>>>(part, S, b_r, T, E, k, topk_idx, topk_w, gap,
+                                                status);
   if (n_launches) *n_launches += 2;
   return cudaGetLastError();
 }
