@@ -15,38 +15,60 @@ namespace {
 // gather, so no atomics and a fixed summation order. A row outside
 // [0, n_rows) (an assignment the dispatch skipped, or bad caller data) adds
 // nothing and latches COLI_EDEVICE; it is never read.
+// A block takes one token and a 1024-column slab, a thread one float4 column:
+// the k row indices and gates are loaded first, then the k rows of every
+// slice (all loads of a slice in flight together), each row summed over the
+// slices in order, then merged with j ascending.
 template <bool BF16_OUT>
 __global__ void __launch_bounds__(256)
     k_combine(const float* __restrict__ part, int splits, size_t part_stride,
               const int32_t* __restrict__ assign_row, const float* __restrict__ topk_w, int T,
               int k, int d, int n_rows, void* __restrict__ y, int* status) {
-  // block (token t, 1024-wide column slab); one float4 column per thread
   const int t = blockIdx.x;
   const int d4 = d / 4;
   const int c = blockIdx.y * blockDim.x + threadIdx.x;
   if (c >= d4) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-  for (int j = 0; j < k; ++j) {
-    const size_t a = static_cast<size_t>(t) * k + j;
-    const float g = topk_w[a];
-    const int row = assign_row[a];
-    if (row < 0 || row >= n_rows) {
-      if (c == 0) latch_error(status, kErrDevice);
-      continue;
+  constexpr int KMAX = 8;
+  int row[KMAX];
+  float g[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    row[j] = -1;
+    g[j] = 0.f;
+    if (j < k) {
+      const size_t a = static_cast<size_t>(t) * k + j;
+      const int r = assign_row[a];
+      g[j] = topk_w[a];
+      if (r >= 0 && r < n_rows) row[j] = r;
+      else if (c == 0) latch_error(status, kErrDevice);
     }
-    const size_t base = static_cast<size_t>(row) * d4 + c;
-    float4 v = reinterpret_cast<const float4*>(part)[base];
-#pragma unroll 4
-    for (int s = 1; s < splits; ++s) {
-      const float4 w = reinterpret_cast<const float4*>(part + s * part_stride)[base];
-      v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
-    }
-    acc.x = fmaf(g, v.x, acc.x);
-    acc.y = fmaf(g, v.y, acc.y);
-    acc.z = fmaf(g, v.z, acc.z);
-    acc.w = fmaf(g, v.w, acc.w);
   }
+  float4 v[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j)
+    v[j] = row[j] >= 0 ? reinterpret_cast<const float4*>(part)[static_cast<size_t>(row[j]) * d4 + c]
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 1; s < splits; ++s) {
+    const float4* ps = reinterpret_cast<const float4*>(part + s * part_stride);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (row[j] >= 0) {
+        const float4 w = ps[static_cast<size_t>(row[j]) * d4 + c];
+        v[j].x += w.x;
+        v[j].y += w.y;
+        v[j].z += w.z;
+        v[j].w += w.w;
+      }
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j)
+    if (row[j] >= 0) {
+      acc.x = fmaf(g[j], v[j].x, acc.x);
+      acc.y = fmaf(g[j], v[j].y, acc.y);
+      acc.z = fmaf(g[j], v[j].z, acc.z);
+      acc.w = fmaf(g[j], v[j].w, acc.w);
+    }
   if (BF16_OUT) {
     uint2 o;
     o.x = pack_bf16x2(acc.x, acc.y);
