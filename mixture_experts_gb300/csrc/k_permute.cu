@@ -210,14 +210,26 @@ __global__ void __launch_bounds__(256)
     }
     const uint4* src = x + static_cast<size_t>(t) * vec_per_row;
     uint4* dst = x_perm + static_cast<size_t>(r) * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) {
-      uint4 u;
-      asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-                   : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
-                   : "l"(src + v), "l"(keep));
-      asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(dst + v),
-                   "r"(u.x), "r"(u.y), "r"(u.z), "r"(u.w), "l"(stream)
-                   : "memory");
+    // up to 8 vectors per lane in flight: all loads of a batch, then its stores
+    constexpr int kBatch = 8;
+    for (int v0 = 0; v0 < vec_per_row; v0 += 32 * kBatch) {
+      uint4 u[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int v = v0 + 32 * b + lane;
+        if (v < vec_per_row)
+          asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                       : "=r"(u[b].x), "=r"(u[b].y), "=r"(u[b].z), "=r"(u[b].w)
+                       : "l"(src + v), "l"(keep));
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int v = v0 + 32 * b + lane;
+        if (v < vec_per_row)
+          asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(dst + v),
+                       "r"(u[b].x), "r"(u[b].y), "r"(u[b].z), "r"(u[b].w), "l"(stream)
+                       : "memory");
+      }
     }
   }
 }
