@@ -24,8 +24,9 @@
 // one 16-byte (E4M3) or 8-byte (E2M1) piece per quarter u whose halves are
 // the stage's units u and 4 + u.
 //
-// Conversion. int4: q * s rounded once to bf16 (as in the bf16-operand
-// kernel). MX: every element is exact in bf16 (an E4M3 or E2M1 value times a
+// Conversion. int4: 136 + q from the nibble (one LOP3 per pair), minus 136
+// (exact), times the group scale: q * s rounded once to bf16. MX: every
+// element is exact in bf16 (an E4M3 or E2M1 value times a
 // power of two) unless the product leaves bf16's range. The hardware turns
 // two codes into an fp16 pair; moving the fp16 exponent field into the low
 // bits of the bf16 one gives the element times 2^-112 exactly (fp16 holds
