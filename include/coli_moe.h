@@ -90,9 +90,9 @@ typedef enum {
  * sum of q*x in fp32 (w = q*s exactly); PREFILL dequantises each weight to a
  * bf16 tensor-core operand, q*s rounded once to nearest even (q*s can need 11
  * significant bits, bf16 holds 8: a relative change of at most 2^-9 per
- * weight). A layer has no PREFILL form (and runs DECODE whatever `path`
- * asks) with 4-bit experts (int4, MXFP4) when d_model or d_ff is 128, or
- * with the residency tier. */
+ * weight). A layer with 4-bit experts (int4, MXFP4) and d_model or d_ff
+ * equal to 128 has no PREFILL form and runs DECODE whatever `path` asks; a
+ * residency-tier layer runs DECODE (PREFILL is rejected at create). */
 typedef enum { COLI_PATH_AUTO = 0, COLI_PATH_DECODE = 1, COLI_PATH_PREFILL = 2 } coli_path;
 
 typedef struct {
