@@ -370,13 +370,27 @@ def roofline(s, path, n_rows, active, avg, ms_fwd, pk, pk_src, config_name):
     return roof
 
 
+def expert_bytes(s) -> int:
+    """Bytes of one expert's three projections in the handle (weights plus
+    their scales): bf16 / f32 elements, int4 nibbles with a bf16 scale per 128,
+    MX codes with an E8M0 byte per 32."""
+    n = 3 * s.f * s.d  # weights of gate, up and down
+    if s.wdt == "i4g128":
+        return n // 2 + (n // 128) * 2
+    if s.wdt == "mxfp8":
+        return n + n // 32
+    if s.wdt == "mxfp4":
+        return n // 2 + n // 32
+    return n * (4 if s.wdt == "f32" else 2)
+
+
 def tier_record(s, layer, counts, avg, pk, torch):
     """Residency tier: bytes each forward reads from HBM slots and from host
     memory over NVLink-C2C, the FFN's effective host-read rate (host bytes /
     (FFN time - HBM bytes at the HBM peak)), and a pinned host -> device copy
     of 1 GiB timed in the same process as the reference rate."""
     slots, _ = layer.residency()
-    per = 3 * s.f * s.d * 2 if s.wdt == "bf16" else None
+    per = expert_bytes(s)
     active = [e for e in range(s.E) if counts[e] > 0]
     hbm = sum(per for e in active if slots[e] >= 0)
     host = sum(per for e in active if slots[e] < 0)

@@ -152,3 +152,17 @@ def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
     assert bench.traffic_record("mixtral_decode", "dec") == 123
     assert bench.traffic_record("mixtral_prefill", "tc") is None  # sources changed
     assert bench.traffic_record("skewed", "tc") is None  # never captured
+
+
+@pytest.mark.parametrize("wdt,per_weight", [("bf16", 2.0), ("f32", 4.0),
+                                            ("i4g128", 0.5 + 2.0 / 128),
+                                            ("mxfp8", 1.0 + 1.0 / 32),
+                                            ("mxfp4", 0.5 + 1.0 / 32)])
+def test_expert_bytes_per_format(wdt, per_weight):
+    """One expert's bytes in the handle: 3·f·d weights at the format's width
+    plus its scales (int4: a bf16 per 128; MX: an E8M0 byte per 32)."""
+    import bench
+    from mixture_experts_gb300 import inputs
+    s = inputs.MoEShape("x", T=32, d=4096, E=8, k=2, f=14336, wdt=wdt,
+                        act="f32" if wdt == "f32" else "bf16")
+    assert bench.expert_bytes(s) == 3 * 14336 * 4096 * per_weight
